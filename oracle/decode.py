@@ -1,0 +1,217 @@
+"""Float64 decode step of a block-quantized Llama decoder (test infrastructure; see package doc).
+
+Per layer ("EdgeRunner Core Architecture" section 5.1, decode case of one token
+per sequence):
+
+  h  = rmsnorm(x, attn_norm)
+  q, k, v = Wq h, Wk h, Wv h
+  q, k = rope(q, pos), rope(k, pos)                       (section 7)
+  Kc[pos], Vc[pos] = fp16(k), fp16(v)                     (section 4.3: K/V written
+                                                           at row `pos`, fp16 cache)
+  o  = GQA attention of q over Kc[0..pos], Vc[0..pos]     (section 5.2)
+  x  = x + Wo o
+  h2 = rmsnorm(x, ffn_norm)
+  x  = x + Wdown (silu(Wgate h2) * (Wup h2))              (section 8)
+
+then logits = Wout rmsnorm(x, output_norm) and the greedy token is the argmax
+(section 2.3, greedyToken with a hasNonFinite flag).  The embedding is a row of
+token_embd; with a tied head that same matrix is the output projection (alpaca.swift
+README, "Capabilities": tied or untied output head).
+
+Readings where the pages are silent (each listed in the design notes):
+  * cached K rows are post-RoPE keys; V is not rotated;
+  * argmax ties go to the lowest index, NaN never wins, any non-finite logit
+    sets the flag;
+  * prefilled cache rows are given, already in cache form (fp16).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Callable, Mapping
+
+import numpy as np
+
+from .blocks import dequant, dequant_rows
+from .ops import attention_gqa, matvec, rmsnorm, rope, swiglu
+
+
+@dataclasses.dataclass(frozen=True)
+class OracleConfig:
+    n_layers: int
+    dim: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ffn_dim: int
+    vocab: int
+    rope_base: float
+    rms_eps: float
+    w_type: str
+    tied: bool
+
+    @property
+    def qd(self) -> int:
+        return self.n_heads * self.head_dim
+
+    @property
+    def kvd(self) -> int:
+        return self.n_kv_heads * self.head_dim
+
+
+class OracleModel:
+    """Config plus a tensor source.
+
+    `tensors` maps GGUF names ("blk.{l}.attn_q.weight", "token_embd.weight", ...)
+    to stored arrays: float32 gains, float16 embedding, or uint8 block bytes.
+    It may be a lazy mapping (only `__getitem__` is used).  With
+    `cache_dequant`, each dequantised matrix is kept after first use.
+    """
+
+    def __init__(self, cfg: OracleConfig, tensors: Mapping[str, np.ndarray] | Callable[[str], np.ndarray],
+                 cache_dequant: bool = False):
+        self.cfg = cfg
+        self._get = tensors if callable(tensors) else tensors.__getitem__
+        self._cache: dict[str, np.ndarray] | None = {} if cache_dequant else None
+
+    def _shape(self, name: str) -> tuple[str, int, int]:
+        c = self.cfg
+        leaf = name.split(".")[-2] if name.startswith("blk.") else name.split(".")[0]
+        shapes = {
+            "attn_q": (c.qd, c.dim), "attn_k": (c.kvd, c.dim), "attn_v": (c.kvd, c.dim),
+            "attn_output": (c.dim, c.qd), "ffn_gate": (c.ffn_dim, c.dim), "ffn_up": (c.ffn_dim, c.dim),
+            "ffn_down": (c.dim, c.ffn_dim), "output": (c.vocab, c.dim), "token_embd": (c.vocab, c.dim),
+        }
+        kind = c.w_type
+        if leaf == "token_embd" and not c.tied:
+            kind = "f16"
+        return (kind,) + shapes[leaf]
+
+    def matrix(self, name: str) -> np.ndarray:
+        if self._cache is not None and name in self._cache:
+            return self._cache[name]
+        kind, rows, cols = self._shape(name)
+        w = dequant(self._get(name), kind, rows, cols)
+        if self._cache is not None:
+            self._cache[name] = w
+        return w
+
+    def gain(self, name: str) -> np.ndarray:
+        return np.asarray(self._get(name), dtype=np.float32).astype(np.float64)
+
+    def embedding_rows(self, tokens) -> np.ndarray:
+        kind, rows, cols = self._shape("token_embd.weight")
+        return dequant_rows(self._get("token_embd.weight"), kind, rows, cols, tokens)
+
+    def head_name(self) -> str:
+        return "token_embd.weight" if self.cfg.tied else "output.weight"
+
+
+class OracleCache:
+    """fp16 K and V rows per (sequence, layer): arrays [capacity, n_kv_heads, head_dim]."""
+
+    def __init__(self, cfg: OracleConfig, batch: int, capacity: int):
+        self.cfg, self.batch, self.capacity = cfg, batch, capacity
+        shp = (capacity, cfg.n_kv_heads, cfg.head_dim)
+        self.k = [[np.zeros(shp, np.float16) for _ in range(cfg.n_layers)] for _ in range(batch)]
+        self.v = [[np.zeros(shp, np.float16) for _ in range(cfg.n_layers)] for _ in range(batch)]
+
+    def fill(self, b: int, layer: int, k_rows: np.ndarray, v_rows: np.ndarray, start: int = 0) -> None:
+        """Copy token-major rows [n, n_kv_heads*head_dim] into rows start..start+n-1."""
+        n = k_rows.shape[0]
+        c = self.cfg
+        self.k[b][layer][start:start + n] = np.asarray(k_rows, np.float16).reshape(n, c.n_kv_heads, c.head_dim)
+        self.v[b][layer][start:start + n] = np.asarray(v_rows, np.float16).reshape(n, c.n_kv_heads, c.head_dim)
+
+
+def _argmax_flag(logits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    finite = np.isfinite(logits)
+    nonfinite = ~finite.all(axis=-1)
+    clean = np.where(np.isnan(logits), -np.inf, logits)
+    return np.argmax(clean, axis=-1).astype(np.int64), nonfinite
+
+
+def decode_step(model: OracleModel, cache: OracleCache, tokens, positions,
+                seqs=None) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """One decode step for every sequence b (or only `seqs`): token tokens[b] at position positions[b].
+
+    Writes the new K/V rows into `cache` and returns (logits [B, vocab] float64,
+    argmax [B], non_finite [B]) for the sequences computed (in `seqs` order).
+    """
+    c = model.cfg
+    seqs = list(range(len(tokens))) if seqs is None else list(seqs)
+    tok = np.asarray(tokens)[seqs]
+    pos = np.asarray(positions)[seqs]
+    B = len(seqs)
+    x = model.embedding_rows(tok)                                   # [B, dim]
+    for l in range(c.n_layers):
+        p = f"blk.{l}."
+        h = rmsnorm(x, model.gain(p + "attn_norm.weight"), c.rms_eps)
+        q = matvec(model.matrix(p + "attn_q.weight"), h)           # [B, qd]
+        k = matvec(model.matrix(p + "attn_k.weight"), h)           # [B, kvd]
+        v = matvec(model.matrix(p + "attn_v.weight"), h)
+        o = np.empty((B, c.qd), dtype=np.float64)
+        for i, b in enumerate(seqs):
+            pb = int(pos[i])
+            qh = rope(q[i].reshape(c.n_heads, c.head_dim), pb, c.rope_base)
+            kh = rope(k[i].reshape(c.n_kv_heads, c.head_dim), pb, c.rope_base)
+            cache.k[b][l][pb] = kh.astype(np.float16)
+            cache.v[b][l][pb] = v[i].reshape(c.n_kv_heads, c.head_dim).astype(np.float16)
+            o[i] = attention_gqa(qh, cache.k[b][l][:pb + 1], cache.v[b][l][:pb + 1]).reshape(-1)
+        x = x + matvec(model.matrix(p + "attn_output.weight"), o)
+        h2 = rmsnorm(x, model.gain(p + "ffn_norm.weight"), c.rms_eps)
+        a = swiglu(matvec(model.matrix(p + "ffn_gate.weight"), h2), matvec(model.matrix(p + "ffn_up.weight"), h2))
+        x = x + matvec(model.matrix(p + "ffn_down.weight"), a)
+    hf = rmsnorm(x, model.gain("output_norm.weight"), c.rms_eps)
+    logits = matvec(model.matrix(model.head_name()), hf)
+    am, nf = _argmax_flag(logits)
+    return logits, am, nf
+
+
+def greedy(model: OracleModel, cache: OracleCache, tokens, positions, steps: int, seqs=None):
+    """Chain `steps` greedy decode steps: next token = argmax, position + 1.
+
+    Returns (tokens fed per step [steps, B], logits per step [steps, B, vocab]).
+    """
+    tok = np.array(tokens, dtype=np.int64)
+    pos = np.array(positions, dtype=np.int64)
+    seqs = list(range(len(tok))) if seqs is None else list(seqs)
+    fed, out = [], []
+    for _ in range(steps):
+        fed.append(tok[seqs].copy())
+        logits, am, _ = decode_step(model, cache, tok, pos, seqs=seqs)
+        out.append(logits)
+        tok[seqs] = am
+        pos[seqs] += 1
+    return np.array(fed), np.array(out)
+
+
+def uncached_logits(model: OracleModel, token_seq) -> np.ndarray:
+    """Logits at the last position of `token_seq` (positions 0..n-1) recomputed from scratch.
+
+    Every position's K and V are computed together, rounded to fp16 as the
+    cache would hold them, and each query attends to positions 0..itself.
+    Used to check incremental decoding ("cached == uncached", alpaca.swift README,
+    "Numerical validation", levels 2-4).
+    """
+    c = model.cfg
+    toks = np.asarray(token_seq)
+    n = len(toks)
+    x = model.embedding_rows(toks)                                  # [n, dim]
+    for l in range(c.n_layers):
+        p = f"blk.{l}."
+        h = rmsnorm(x, model.gain(p + "attn_norm.weight"), c.rms_eps)
+        q = matvec(model.matrix(p + "attn_q.weight"), h)
+        k = matvec(model.matrix(p + "attn_k.weight"), h)
+        v = matvec(model.matrix(p + "attn_v.weight"), h)
+        K = np.stack([rope(k[t].reshape(c.n_kv_heads, c.head_dim), t, c.rope_base) for t in range(n)])
+        K = K.astype(np.float16)
+        V = v.reshape(n, c.n_kv_heads, c.head_dim).astype(np.float16)
+        o = np.stack([attention_gqa(rope(q[t].reshape(c.n_heads, c.head_dim), t, c.rope_base),
+                                    K[:t + 1], V[:t + 1]).reshape(-1) for t in range(n)])
+        x = x + matvec(model.matrix(p + "attn_output.weight"), o)
+        h2 = rmsnorm(x, model.gain(p + "ffn_norm.weight"), c.rms_eps)
+        a = swiglu(matvec(model.matrix(p + "ffn_gate.weight"), h2), matvec(model.matrix(p + "ffn_up.weight"), h2))
+        x = x + matvec(model.matrix(p + "ffn_down.weight"), a)
+    hf = rmsnorm(x[-1:], model.gain("output_norm.weight"), c.rms_eps)
+    return matvec(model.matrix(model.head_name()), hf)[0]
