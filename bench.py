@@ -1,0 +1,399 @@
+"""Decode-step benchmark: tok/s and HBM roofline fraction of the block-quantized decode step.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one decode step of every sequence of the workload (embedding, all
+layers, LM head, greedy argmax), replayed as one CUDA graph with tokens and
+positions chained on the device.  Timed: K steps after W warm-up steps, CUDA
+events on the launching stream, barrier + synchronize on both sides, max over
+ranks.  With N > 1 (torchrun) every rank runs an independent replica ("weak"
+scaling; the step has no exchange between GPUs).
+
+--impl reference times the float64 CPU oracle on the same workload (a bounded
+sample of steps) on the host cores and prints the same JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode tok/s per step and achieved HBM GB/s vs 8 TB/s roofline (Q8_0/Q4_0)"
+BPB = {"q8_0": 34, "q4_0": 18}
+
+
+# ----------------------------------------------------------------------------------------------
+# algorithmic bytes (each weight byte once per step, KV rows read once, outputs written once)
+# ----------------------------------------------------------------------------------------------
+def stage_bytes(wl: synth.Workload, pos: np.ndarray) -> dict[str, float]:
+    s = wl.shape
+    bpb = BPB[s.w_type] / 32.0
+    B = wl.batch
+    D, qd, kvd, F, V = s.dim, s.qd, s.kvd, s.ffn_dim, s.vocab
+    attn_rows = float(np.sum(pos + 1))
+    return {
+        "embed": B * D * (2.0 if not s.tied else bpb) + B * D * 4,
+        "qkv": (qd + 2 * kvd) * D * bpb + B * (D * 4 + qd * 4 + 2 * kvd * 2) + D * 4,
+        "attn": attn_rows * kvd * 2 * 2 + B * qd * 4 * 2,
+        "wo": D * qd * bpb + B * (qd * 4 + 2 * D * 4),
+        "gateup": 2 * F * D * bpb + B * (D * 4 + F * 4) + D * 4,
+        "down": D * F * bpb + B * (F * 4 + 2 * D * 4),
+        "head": V * D * bpb + B * (D * 4 + V * 4) + D * 4,
+    }
+
+
+def step_bytes(wl: synth.Workload, pos: np.ndarray) -> float:
+    b = stage_bytes(wl, pos)
+    L = wl.shape.n_layers
+    return b["embed"] + L * (b["qkv"] + b["attn"] + b["wo"] + b["gateup"] + b["down"]) + b["head"]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------------------------
+def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+
+    from block_quantized_token_gb300 import build as libbuild
+    if rank == 0 or not libbuild.up_to_date():
+        libbuild.build()
+    from block_quantized_token_gb300 import er, runtime
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.workload(args.workload)
+    s = wl.shape
+    B = wl.batch
+    K, W = args.steps, args.warmup
+    cap = wl.prefill + max(K, W, 1)
+    wl_run = wl.with_(steps=cap - wl.prefill)
+
+    t0 = time.time()
+    model = runtime.DecodeModel(s, lambda n: synth.weight_tensor(s, n), max_batch=B)
+    state = runtime.DecodeState(model, B, cap)
+    for b in range(B):
+        for l in range(s.n_layers):
+            k, v = synth.kv_prefill(wl_run, b, l)
+            state.write_rows(b, l, k, v)
+    setup_s = time.time() - t0
+
+    stream = torch.cuda.Stream(dev)
+    sp = stream.cuda_stream
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    pos = torch.empty(B, dtype=torch.int32, device=dev)
+    logits = torch.empty((B, s.vocab), dtype=torch.float32, device=dev)
+
+    def reset():
+        tok.copy_(torch.from_numpy(wl.tokens0()))
+        pos.copy_(torch.from_numpy(wl.positions0()))
+
+    def one_step():
+        er.er_decode_step(tok.data_ptr(), pos.data_ptr(), state.handle, logits.data_ptr(), tok.data_ptr(), sp)
+        er.er_positions_increment(pos.data_ptr(), B, sp)
+
+    with torch.cuda.stream(stream):
+        reset()
+        for _ in range(W):
+            one_step()
+        reset()
+    stream.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = ClockSampler(local_rank)
+    if rank == 0:
+        clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(K):
+        one_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1)
+    clock_info = clocks.stop() if rank == 0 else None
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st, code, nf = state.device_error()
+    if code:
+        raise RuntimeError(f"device error flags {code}")
+
+    # ---- end to end through the C ABI with host buffers (pinned), one H2D + D2H per step
+    tok_h = torch.from_numpy(wl.tokens0()).pin_memory()
+    pos_h = torch.from_numpy(wl.positions0()).pin_memory()
+    out_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    argmax_d = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def e2e_step():
+        tok.copy_(tok_h, non_blocking=True)
+        pos.copy_(pos_h, non_blocking=True)
+        er.er_decode_step(tok.data_ptr(), pos.data_ptr(), state.handle, logits.data_ptr(), argmax_d.data_ptr(), sp)
+        out_h.copy_(argmax_d, non_blocking=True)
+        stream.synchronize()
+        tok_h.copy_(out_h)
+        pos_h.add_(1)
+
+    with torch.cuda.stream(stream):
+        for _ in range(min(W, 3)):
+            e2e_step()
+        tok_h.copy_(torch.from_numpy(wl.tokens0()))
+        pos_h.copy_(torch.from_numpy(wl.positions0()))
+        torch.cuda.synchronize(dev)
+        e0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        e2e_s = time.perf_counter() - e0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    # ---- per-stage launch durations (eager launches, L2 flushed before each) for the roofline
+    roof = None
+    if rank == 0:
+        roof = stage_roofline(er, state, wl, tok, pos, logits, stream, dev)
+
+    positions = wl.positions0()[None, :] + np.arange(K)[:, None]
+    bytes_step = float(np.mean([step_bytes(wl, p) for p in positions]))
+    tokens = B * K * world
+    gemv_groups = 1 if B <= 4 else (B + 3) // 4  # column groups per GEMV launch set
+    launches = 1 + s.n_layers * (1 + 4 * gemv_groups) + gemv_groups + 1
+    result = None
+    if rank == 0:
+        result = {
+            "metric": METRIC,
+            "value": tokens / (ms / 1e3),
+            "unit": "tok/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": ms / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "model": f"{s.n_layers}L d{s.dim} {s.n_heads}/{s.n_kv_heads}x{s.head_dim} "
+                                                     f"ffn{s.ffn_dim} V{s.vocab} {s.w_type} "
+                                                     f"{'tied' if s.tied else 'untied'}",
+                       "batch": B, "context": wl.prefill, "chained_steps": K,
+                       "step_bytes": bytes_step, "step_gbs": bytes_step / (ms / K / 1e3) / 1e9,
+                       "step_roofline_frac": bytes_step / (ms / K / 1e3) / 1e9 / measured_peaks()["hbm_gbs"],
+                       "l2": ("inputs larger than L2" if bytes_step > 129e6 else "L2-resident working set"),
+                       "parallelism": f"replicas x{world}", "setup_s": round(setup_s, 1)},
+            "e2e": {"value": tokens / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
+            "gpu_launches": launches * K,
+            "roofline": roof,
+            "clocks": clock_info,
+        }
+    state.close()
+    model.close()
+    return result
+
+
+def stage_roofline(er, state, wl, tok, pos, logits, stream, dev, iters: int = 20) -> dict:
+    """Average event-timed duration of each stage kernel at the workload's first position.
+
+    Every launch is preceded by a write of a 256 MiB buffer (larger than L2), so
+    the weights come from HBM as in the chained step.  Returns the roofline of
+    the stage with the largest total time per step.
+    """
+    import torch
+    peaks = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    pos_np = wl.positions0()
+    sb = stage_bytes(wl, pos_np)
+    L = wl.shape.n_layers
+    per_step = {"qkv": L, "attn": L, "wo": L, "gateup": L, "down": L, "head": 1}
+    ids = {"qkv": er.ER_STAGE_QKV, "attn": er.ER_STAGE_ATTN, "wo": er.ER_STAGE_WO, "gateup": er.ER_STAGE_GATEUP,
+           "down": er.ER_STAGE_DOWN, "head": er.ER_STAGE_HEAD}
+    sp = stream.cuda_stream
+    durs = {}
+    with torch.cuda.stream(stream):
+        tok.copy_(torch.from_numpy(wl.tokens0()))
+        pos.copy_(torch.from_numpy(pos_np))
+        for name, sid in ids.items():
+            tot = 0.0
+            for i in range(iters + 2):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                er.er_launch_stage(state.handle, sid, L // 2, tok.data_ptr(), pos.data_ptr(), logits.data_ptr(),
+                                   None, sp)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    tot += e0.elapsed_time(e1)
+            durs[name] = tot / iters
+    share = {n: durs[n] * per_step[n] for n in durs}
+    top = max(share, key=share.get)
+    achieved = sb[top] / (durs[top] / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "peak_source": f"{peaks['source']} hbm_gbs (burst, kernel timed alone)",
+            "bytes_per_launch": sb[top], "us_per_launch": durs[top] * 1e3,
+            "stages_us": {n: round(d * 1e3, 2) for n, d in durs.items()},
+            "stages_gbs": {n: round(sb[n] / (durs[n] / 1e3) / 1e9, 1) for n in durs}}
+
+
+# ----------------------------------------------------------------------------------------------
+# the oracle arm (CPU, float64)
+# ----------------------------------------------------------------------------------------------
+def oracle_sample(wl: synth.Workload, steps: int, budget_s: float, seqs=None) -> tuple[float, int, dict]:
+    """Time the oracle (as it stands) on consecutive steps of the workload; returns (tok/s, steps, info)."""
+    import oracle
+    s = wl.shape
+    seqs = list(range(wl.batch)) if seqs is None else seqs
+    ocfg = oracle.OracleConfig(**{k: getattr(s, k) for k in oracle.OracleConfig.__dataclass_fields__})
+    cache = oracle.OracleCache(ocfg, wl.batch, wl.prefill + steps)
+    for b in seqs:
+        for l in range(s.n_layers):
+            k, v = synth.kv_prefill(wl, b, l)
+            cache.fill(b, l, k, v)
+    model = oracle.OracleModel(ocfg, lambda n: synth.weight_tensor(s, n))
+    tok, pos = wl.tokens0().astype(np.int64), wl.positions0().astype(np.int64)
+    t0 = time.perf_counter()
+    done = 0
+    for _ in range(steps):
+        _, am, _ = oracle.decode_step(model, cache, tok, pos, seqs=seqs)
+        tok[seqs] = am
+        pos[seqs] += 1
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return len(seqs) * done / el, done, {"seconds": el}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="smollm_q8", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = synth.workload(args.workload)
+    cores = os.cpu_count()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = max(10.0, min(60.0, args.cpu_budget * 2))
+        tps, done, info = oracle_sample(wl, args.steps, budget, seqs=[0])
+        sample = f"{done} consecutive steps of sequence 0 from position {wl.prefill} (of {args.steps} requested)"
+        line = {"metric": METRIC, "value": tps, "unit": "tok/s", "n_gpus": args.gpus, "steps": done,
+                "warmup": 0, "ms_per_step": info["seconds"] * 1e3 / max(done, 1), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": wl.name, "batch": wl.batch, "context": wl.prefill},
+                "impl": "reference",
+                "cpu_baseline": {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": tps, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.no_cpu_baseline:
+            res["cpu_baseline"] = None
+        else:
+            tps, done, info = oracle_sample(wl, 8, args.cpu_budget, seqs=[0])
+            res["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                   "sample": f"{done} consecutive steps of sequence 0 from position {wl.prefill} "
+                                             f"({info['seconds']:.1f} s, numpy float64, BLAS on all cores)"}
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

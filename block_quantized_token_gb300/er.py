@@ -1,0 +1,189 @@
+"""ctypes binding of liber.so: the same names as include/er.h, argument marshalling only.
+
+Every function raises ErError when the C call returns a status other than
+ER_OK.  Device pointers are plain integers (e.g. ``tensor.data_ptr()``) and
+streams are ``cudaStream_t`` values as integers (e.g.
+``torch.cuda.current_stream().cuda_stream``).  Importing this module loads the
+library; it fails loudly when the library has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liber.so")
+
+ER_OK, ER_EINVAL, ER_ENOMEM, ER_ECUDA, ER_EUNSUPPORTED, ER_EDEVICE = range(6)
+ER_F32, ER_F16, ER_Q4_0, ER_Q8_0 = 0, 1, 2, 8
+DTYPES = {"f32": ER_F32, "f16": ER_F16, "q4_0": ER_Q4_0, "q8_0": ER_Q8_0}
+(ER_STAGE_EMBED, ER_STAGE_QKV, ER_STAGE_ATTN, ER_STAGE_WO, ER_STAGE_GATEUP, ER_STAGE_DOWN,
+ ER_STAGE_HEAD) = range(7)
+
+
+class ErError(RuntimeError):
+    def __init__(self, msg: str, status: int):
+        super().__init__(msg)
+        self.status = status
+
+
+class er_config(ctypes.Structure):
+    _fields_ = [("dim", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rope_base", ctypes.c_double), ("rms_eps", ctypes.c_double),
+                ("w_type", ctypes.c_int32), ("tied", ctypes.c_int32), ("max_batch", ctypes.c_int32)]
+
+
+class er_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+class er_weights(ctypes.Structure):
+    _fields_ = [("tok_embd", ctypes.c_void_p), ("output_norm", ctypes.c_void_p), ("output", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(er_layer_weights))]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with block_quantized_token_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_void_p
+    sigs = {
+        "er_model_create": (I32, [P(er_config), P(er_weights), VP, P(VP)]),
+        "er_model_destroy": (None, [VP]),
+        "er_model_device_bytes": (ctypes.c_size_t, [VP]),
+        "er_kv_create": (I32, [VP, I32, I32, P(VP)]),
+        "er_kv_destroy": (None, [VP]),
+        "er_kv_layer_ptrs": (I32, [VP, I32, I32, P(VP), P(VP)]),
+        "er_kv_write": (I32, [VP, I32, I32, I32, I32, VP, VP, VP]),
+        "er_kv_read": (I32, [VP, I32, I32, I32, I32, VP, VP, VP]),
+        "er_decode_step": (I32, [VP, VP, VP, VP, VP, VP]),
+        "er_decode_step_eager": (I32, [VP, VP, VP, VP, VP, VP]),
+        "er_positions_increment": (I32, [VP, I32, VP]),
+        "er_get_device_error": (I32, [VP, P(I32), P(I32)]),
+        "er_launch_stage": (I32, [VP, I32, I32, VP, VP, VP, VP, VP]),
+        "er_matrix_create": (I32, [I32, I32, I32, VP, VP, P(VP)]),
+        "er_matrix_destroy": (None, [VP]),
+        "er_matrix_dequant": (I32, [VP, VP, VP]),
+        "er_matrix_gemv": (I32, [VP, VP, I32, VP, VP]),
+        "er_status_str": (ctypes.c_char_p, [I32]),
+        "er_last_error": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_kv_create", "er_kv_destroy",
+            "er_kv_layer_ptrs", "er_kv_write", "er_kv_read", "er_decode_step", "er_decode_step_eager", "er_positions_increment",
+            "er_get_device_error", "er_launch_stage", "er_matrix_create", "er_matrix_destroy",
+            "er_matrix_dequant", "er_matrix_gemv", "er_status_str", "er_last_error")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != ER_OK:
+        raise ErError(f"{what}: {er_status_str(status)}: {er_last_error()}", status)
+
+
+def er_status_str(status: int) -> str:
+    return _lib.er_status_str(status).decode()
+
+
+def er_last_error() -> str:
+    return _lib.er_last_error().decode()
+
+
+def er_model_create(cfg: er_config, weights: er_weights, stream: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.er_model_create(ctypes.byref(cfg), ctypes.byref(weights), stream, ctypes.byref(out)),
+           "er_model_create")
+    return out.value
+
+
+def er_model_destroy(model: int) -> None:
+    _lib.er_model_destroy(model)
+
+
+def er_model_device_bytes(model: int) -> int:
+    return _lib.er_model_device_bytes(model)
+
+
+def er_kv_create(model: int, batch: int, capacity: int) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.er_kv_create(model, batch, capacity, ctypes.byref(out)), "er_kv_create")
+    return out.value
+
+
+def er_kv_destroy(kv: int) -> None:
+    _lib.er_kv_destroy(kv)
+
+
+def er_kv_layer_ptrs(kv: int, seq: int, layer: int) -> tuple[int, int]:
+    k, v = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(_lib.er_kv_layer_ptrs(kv, seq, layer, ctypes.byref(k), ctypes.byref(v)), "er_kv_layer_ptrs")
+    return k.value, v.value
+
+
+def er_kv_write(kv: int, seq: int, layer: int, start: int, n: int, k_rows: int, v_rows: int,
+                stream: int = 0) -> None:
+    _check(_lib.er_kv_write(kv, seq, layer, start, n, k_rows, v_rows, stream), "er_kv_write")
+
+
+def er_kv_read(kv: int, seq: int, layer: int, start: int, n: int, k_rows: int, v_rows: int,
+               stream: int = 0) -> None:
+    _check(_lib.er_kv_read(kv, seq, layer, start, n, k_rows, v_rows, stream), "er_kv_read")
+
+
+def er_decode_step(tokens: int, positions: int, kv: int, logits: int | None, argmax: int | None,
+                   stream: int = 0) -> None:
+    _check(_lib.er_decode_step(tokens, positions, kv, logits, argmax, stream), "er_decode_step")
+
+
+def er_decode_step_eager(tokens: int, positions: int, kv: int, logits: int | None, argmax: int | None,
+                         stream: int = 0) -> None:
+    _check(_lib.er_decode_step_eager(tokens, positions, kv, logits, argmax, stream), "er_decode_step_eager")
+
+
+def er_positions_increment(positions: int, batch: int, stream: int = 0) -> None:
+    _check(_lib.er_positions_increment(positions, batch, stream), "er_positions_increment")
+
+
+def er_get_device_error(kv: int) -> tuple[int, int, int]:
+    """Returns (status, code, non_finite) without raising on ER_EDEVICE."""
+    code, nf = ctypes.c_int32(), ctypes.c_int32()
+    st = _lib.er_get_device_error(kv, ctypes.byref(code), ctypes.byref(nf))
+    if st not in (ER_OK, ER_EDEVICE):
+        _check(st, "er_get_device_error")
+    return st, code.value, nf.value
+
+
+def er_launch_stage(kv: int, stage: int, layer: int, tokens: int, positions: int, logits: int | None,
+                    argmax: int | None, stream: int = 0) -> None:
+    _check(_lib.er_launch_stage(kv, stage, layer, tokens, positions, logits, argmax, stream), "er_launch_stage")
+
+
+def er_matrix_create(w_type: int, rows: int, cols: int, blocks: int, stream: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.er_matrix_create(w_type, rows, cols, blocks, stream, ctypes.byref(out)), "er_matrix_create")
+    return out.value
+
+
+def er_matrix_destroy(mat: int) -> None:
+    _lib.er_matrix_destroy(mat)
+
+
+def er_matrix_dequant(mat: int, out: int, stream: int = 0) -> None:
+    _check(_lib.er_matrix_dequant(mat, out, stream), "er_matrix_dequant")
+
+
+def er_matrix_gemv(mat: int, x: int, batch: int, y: int, stream: int = 0) -> None:
+    _check(_lib.er_matrix_gemv(mat, x, batch, y, stream), "er_matrix_gemv")

@@ -1,0 +1,199 @@
+/*
+ * er.h -- C ABI of liber.so: one decode step of a Llama-style decoder whose 2-D
+ * weights are GGUF Q8_0 or Q4_0 blocks, on one NVIDIA GB300 (sm_103a).
+ *
+ * The step follows "EdgeRunner Core Architecture", Overview and section 5.1:
+ *
+ *   tokens -> embedding -> [RMSNorm -> Q/K/V -> RoPE + K/V append -> GQA
+ *   attention -> Wo + residual -> RMSNorm -> SwiGLU FFN + residual] x N ->
+ *   RMSNorm -> LM head -> logits -> greedy argmax
+ *
+ * Conventions for every call:
+ *   - Pointers named *_dev are device memory of the current CUDA device; all
+ *     other pointers are host memory.  `stream` is a cudaStream_t passed as
+ *     void* (NULL = the legacy default stream).
+ *   - Calls return er_status.  Arguments are checked on the host before any
+ *     work is queued; a failed check returns ER_EINVAL / ER_EUNSUPPORTED and
+ *     queues nothing.  A failed CUDA call returns ER_ECUDA.  er_last_error()
+ *     gives a one-line description of the last failure on the calling thread.
+ *   - Work is queued asynchronously on `stream`; no call below synchronises
+ *     the device unless its comment says so.
+ *   - No call throws; no call aborts the process.
+ */
+#ifndef ER_H
+#define ER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ER_API __attribute__((visibility("default")))
+#else
+#define ER_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ER_OK = 0,
+    ER_EINVAL = 1,        /* bad argument (NULL, size out of range, mismatch)   */
+    ER_ENOMEM = 2,        /* device allocation failed                           */
+    ER_ECUDA = 3,         /* a CUDA runtime call failed                         */
+    ER_EUNSUPPORTED = 4,  /* valid but not implemented (e.g. head_dim 96)       */
+    ER_EDEVICE = 5        /* a kernel flagged bad data (see er_get_device_error) */
+} er_status;
+
+/* Tensor storage types.  The numeric values are GGUF's type codes as listed in
+ * "EdgeRunner Core Architecture" section 1.3 (TensorDataType): float32 = 0,
+ * float16 = 1, q4_0 = 2 (18-byte blocks), q8_0 = 8 (34-byte blocks). */
+typedef enum { ER_F32 = 0, ER_F16 = 1, ER_Q4_0 = 2, ER_Q8_0 = 8 } er_dtype;
+
+/* Model shape ("EdgeRunner Core Architecture" section 1.1, LlamaConfig).
+ *   dim        embedding width D
+ *   n_layers   decoder layers L
+ *   n_heads    query heads H;  n_kv_heads  KV heads (H % n_kv_heads == 0)
+ *   head_dim   hd; supported: 64 and 128
+ *   ffn_dim    SwiGLU hidden width F
+ *   vocab      V
+ *   rope_base  RoPE frequency base (angle of pair i at position p: p * base^(-2i/hd))
+ *   rms_eps    RMSNorm epsilon (inside the square root)
+ *   w_type     ER_Q8_0 or ER_Q4_0: the format of every 2-D weight
+ *   tied       0: token_embd is fp16 [V x D] and `output` is a w_type [V x D]
+ *                 head;  1: token_embd is a w_type [V x D] matrix used both
+ *                 as the embedding table and as the head (output must be NULL)
+ *   max_batch  largest batch an er_kv of this model may hold (1..16)
+ * D, H*hd, n_kv_heads*hd and F must be multiples of 32 (whole blocks). */
+typedef struct {
+    int32_t dim, n_layers, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+    double rope_base;
+    double rms_eps;
+    int32_t w_type;
+    int32_t tied;
+    int32_t max_batch;
+} er_config;
+
+/* Device pointers to one layer's tensors in GGUF layout.  Norm gains are fp32
+ * [D].  Matrices are [rows = outputs] x [cols = inputs], row-major, each row
+ * cols/32 consecutive blocks ("EdgeRunner Core Architecture" section 3.2):
+ *   wq [H*hd x D], wk/wv [KV*hd x D], wo [D x H*hd],
+ *   w_gate/w_up [F x D], w_down [D x F]. */
+typedef struct {
+    const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+} er_layer_weights;
+
+/* tok_embd: see er_config.tied; output_norm: fp32 [D]; output: w_type [V x D]
+ * head or NULL when tied; layers: HOST array of n_layers entries. */
+typedef struct {
+    const void *tok_embd, *output_norm, *output;
+    const er_layer_weights *layers;
+} er_weights;
+
+typedef struct er_model er_model;
+typedef struct er_kv er_kv;
+typedef struct er_matrix er_matrix;
+
+/* Builds a model on the current device.  Every weight is repacked from GGUF
+ * blocks into the library's own 16-byte-aligned tiled layout (the same bytes,
+ * rearranged) in model-owned memory; norm gains and the fp16 embedding are
+ * copied.  Synchronises `stream` before returning, so the caller may free its
+ * copies afterwards.  *out is set only on ER_OK. */
+ER_API er_status er_model_create(const er_config *cfg, const er_weights *w, void *stream, er_model **out);
+ER_API void er_model_destroy(er_model *m);
+/* Bytes of device memory the model owns (repacked weights, gains, embedding). */
+ER_API size_t er_model_device_bytes(const er_model *m);
+
+/* Creates the decode state of `batch` independent sequences with room for
+ * `capacity` positions each: the fp16 K/V cache (zeroed), a RoPE cos/sin table
+ * for positions 0..capacity-1 (computed in double on the host, stored fp32),
+ * activations and kernel scratch.  Synchronises the device.  An er_kv must
+ * not outlive its model. */
+ER_API er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out);
+ER_API void er_kv_destroy(er_kv *kv);
+
+/* Device addresses of the K and V cache of sequence `seq`, layer `layer`.
+ * Layout of each: fp16 [n_kv_heads][capacity][head_dim] (head-major, then
+ * position, then dimension).  K rows hold keys after RoPE; V rows are not
+ * rotated.  Callers prefill rows below a sequence's first position here. */
+ER_API er_status er_kv_layer_ptrs(er_kv *kv, int32_t seq, int32_t layer, void **k_dev, void **v_dev);
+
+/* Copy n token-major rows k_rows_dev / v_rows_dev (fp16 [n][n_kv_heads*head_dim],
+ * heads contiguous within a row, the layout GGUF runtimes use) into cache rows
+ * start..start+n-1 of sequence `seq`, layer `layer` (er_kv_write), or the
+ * reverse (er_kv_read).  Queued on `stream`; no synchronisation. */
+ER_API er_status er_kv_write(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n, const void *k_rows_dev,
+                             const void *v_rows_dev, void *stream);
+ER_API er_status er_kv_read(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n, void *k_rows_dev,
+                            void *v_rows_dev, void *stream);
+
+/* One decode step for every sequence b of kv:
+ *   tokens_dev[b]     int32 token id of sequence b (0 <= id < vocab)
+ *   positions_dev[b]  int32 position p of that token (0 <= p < capacity)
+ * Writes K/V of each sequence at row p, attends rows 0..p (rows below p must
+ * hold earlier keys/values), and writes
+ *   logits_dev  fp32 [batch][vocab] (may be NULL)
+ *   argmax_dev  int32 [batch]: greedy token = index of the largest logit,
+ *               lowest index on ties, NaN never chosen (may be NULL; may
+ *               alias tokens_dev to chain steps on the device).
+ * The step runs as one CUDA graph: the first call with a given set of pointers
+ * records it (on a stream the library owns) and later calls replay it.  It
+ * allocates no device memory after the first call for a pointer set and never
+ * synchronises.  A token or position out of range sets a device error flag
+ * (er_get_device_error) and leaves that sequence's outputs unspecified; no
+ * out-of-range memory is touched.  Any non-finite logit sets the non-finite
+ * flag (mirrors greedyToken's hasNonFinite, "EdgeRunner Core Architecture"
+ * section 2.3). */
+ER_API er_status er_decode_step(const int32_t *tokens_dev, const int32_t *positions_dev, er_kv *kv,
+                         float *logits_dev, int32_t *argmax_dev, void *stream);
+/* The same kernels queued directly (no graph); for debugging and tests. */
+ER_API er_status er_decode_step_eager(const int32_t *tokens_dev, const int32_t *positions_dev, er_kv *kv,
+                               float *logits_dev, int32_t *argmax_dev, void *stream);
+
+/* positions_dev[b] += 1 for b < batch (chains steps without a host round trip). */
+ER_API er_status er_positions_increment(int32_t *positions_dev, int32_t batch, void *stream);
+
+/* Synchronises the device, then reports and clears kv's device flags:
+ *   *code        bit 0: a token was out of range; bit 1: a position was out of
+ *                range; bit 2: a pipeline wait in a kernel gave up (internal
+ *                error); 0 if none
+ *   *non_finite  1 if any logit since the last call was NaN or infinite
+ * Returns ER_EDEVICE if *code != 0, else ER_OK. */
+ER_API er_status er_get_device_error(er_kv *kv, int32_t *code, int32_t *non_finite);
+
+/* Stage kernels of the step, queued alone with the step's own arguments for
+ * layer `layer` (ignored by EMBED and HEAD).  For per-kernel timing. */
+typedef enum {
+    ER_STAGE_EMBED = 0,   /* token row -> residual x                          */
+    ER_STAGE_QKV = 1,     /* RMSNorm + [Wq;Wk;Wv] + RoPE + K/V append          */
+    ER_STAGE_ATTN = 2,    /* split-K GQA attention + combine                   */
+    ER_STAGE_WO = 3,      /* Wo + residual                                     */
+    ER_STAGE_GATEUP = 4,  /* RMSNorm + [Wgate;Wup] + SwiGLU                    */
+    ER_STAGE_DOWN = 5,    /* Wdown + residual                                  */
+    ER_STAGE_HEAD = 6     /* final RMSNorm + LM head + argmax                  */
+} er_stage;
+ER_API er_status er_launch_stage(er_kv *kv, int32_t stage, int32_t layer, const int32_t *tokens_dev,
+                          const int32_t *positions_dev, float *logits_dev, int32_t *argmax_dev, void *stream);
+
+/* Stand-alone block-quantized matrix ("EdgeRunner Core Architecture" section
+ * 3.4, tier 1: the raw blocks feed the product directly).  `blocks_dev` is a
+ * GGUF [rows x cols] matrix of type w_type (ER_Q8_0 / ER_Q4_0); it is repacked
+ * into memory the er_matrix owns (synchronises `stream`). */
+ER_API er_status er_matrix_create(int32_t w_type, int32_t rows, int32_t cols, const void *blocks_dev, void *stream,
+                           er_matrix **out);
+ER_API void er_matrix_destroy(er_matrix *mat);
+/* out_dev fp32 [rows][cols] = d * q of every element, from the repacked bytes
+ * (exact: each value has at most 19 significant bits). */
+ER_API er_status er_matrix_dequant(const er_matrix *mat, float *out_dev, void *stream);
+/* y_dev fp32 [batch][rows] = W x_b for x_dev fp32 [batch][cols], 1 <= batch <= 16.
+ * One pass over the weights serves up to 4 batch columns (fewer for very wide
+ * rows).  fp32 activations, fp32 accumulation; deterministic. */
+ER_API er_status er_matrix_gemv(const er_matrix *mat, const float *x_dev, int32_t batch, float *y_dev, void *stream);
+
+ER_API const char *er_status_str(er_status s);
+ER_API const char *er_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ER_H */

@@ -1,0 +1,219 @@
+"""GPU parity of the whole decode step (C ABI) against the float64 oracle.
+
+Gates: logits max |err| <= 2e-3 and relative L2 <= 1e-4 per step; greedy tokens
+identical over the chained steps; appended K/V rows within 1 fp16 ulp (the two
+sides round fp32 / float64 values of k and v to fp16, so a value on a rounding
+boundary may land on either neighbour).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (TINY, gpu_chain, gpu_model, gpu_state, logits_close, oracle_cache, oracle_config,
+                     oracle_model, top2_gap)
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _er():
+    from block_quantized_token_gb300 import er
+    return er
+
+
+class Setup:
+    def __init__(self, wl, max_batch=None, seqs=None):
+        self.wl = wl
+        self.weights = synth.gen.model_weights(wl.shape)
+        self.model = gpu_model(wl.shape, self.weights, max_batch=max_batch or wl.batch)
+        self.state = gpu_state(self.model, wl)
+        self.om = oracle_model(wl.shape, self.weights)
+
+    def ocache(self, seqs=None):
+        return oracle_cache(self.wl, seqs)
+
+    def reset_kv(self):
+        """Rewrite the prefill rows (tests that step at low positions overwrite them)."""
+        for b in range(self.wl.batch):
+            for l in range(self.wl.shape.n_layers):
+                k, v = synth.kv_prefill(self.wl, b, l)
+                self.state.write_rows(b, l, k, v)
+
+    def close(self):
+        self.state.close()
+        self.model.close()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    s = Setup(synth.workload("tiny").with_(steps=4))
+    yield s
+    s.close()
+
+
+def _step(state, wl, tokens, positions, graph=True):
+    dev = state.model.device
+    t = torch.tensor(tokens, dtype=torch.int32, device=dev)
+    p = torch.tensor(positions, dtype=torch.int32, device=dev)
+    lg = torch.empty((wl.batch, wl.shape.vocab), dtype=torch.float32, device=dev)
+    am = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+    state.step(t, p, lg, am, graph=graph)
+    torch.cuda.synchronize()
+    return lg.cpu().numpy().astype(np.float64), am.cpu().numpy()
+
+
+def test_tiny_single_step(tiny):
+    """2-layer Q8_0 model, token 7 at position 16 over a 16-row prefill."""
+    wl = tiny.wl
+    got, am = _step(tiny.state, wl, wl.tokens0(), wl.positions0())
+    oc = tiny.ocache()
+    want, oam, onf = oracle.decode_step(tiny.om, oc, wl.tokens0(), wl.positions0())
+    logits_close(got, want)
+    assert list(am) == list(oam), f"top-2 gap {top2_gap(want[0]):.3e}"
+    assert not onf.any()
+    # the appended rows (post-RoPE K, V) against the oracle's fp16 rows
+    p = wl.prefill
+    for l in range(wl.shape.n_layers):
+        k, v = tiny.state.read_rows(0, l, p, 1)
+        ok = oc.k[0][l][p].reshape(-1).astype(np.float32)
+        ov = oc.v[0][l][p].reshape(-1).astype(np.float32)
+        for g, w in ((k, ok), (v, ov)):
+            g = g.cpu().numpy().reshape(-1).astype(np.float32)
+            ulp = np.abs(np.spacing(w.astype(np.float16)).astype(np.float32))
+            assert (np.abs(g - w) <= ulp).all()
+    st, code, nf = tiny.state.device_error()
+    assert code == 0 and nf == 0
+
+
+def test_graph_equals_eager_and_deterministic(tiny):
+    wl = tiny.wl
+    a, am_a = _step(tiny.state, wl, wl.tokens0(), wl.positions0(), graph=True)
+    b, am_b = _step(tiny.state, wl, wl.tokens0(), wl.positions0(), graph=False)
+    c, am_c = _step(tiny.state, wl, wl.tokens0(), wl.positions0(), graph=True)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(a, c)
+    assert list(am_a) == list(am_b) == list(am_c)
+
+
+def test_tiny_chain(tiny):
+    """Four chained greedy steps (tokens fed back on the device)."""
+    wl = tiny.wl
+    fed, hist = gpu_chain(tiny.state, wl, 4)
+    ofed, ohist = oracle.greedy(tiny.om, tiny.ocache(), wl.tokens0(), wl.positions0(), 4)
+    np.testing.assert_array_equal(fed, ofed)
+    for s in range(4):
+        logits_close(hist[s], ohist[s])
+
+
+@pytest.mark.parametrize("pos", [0, 1, 15, 16, 19])
+def test_positions_edge(tiny, pos):
+    """Position 0 (one row attended), the prefill boundary and the last row of the cache (19)."""
+    tiny.reset_kv()
+    got, am = _step(tiny.state, tiny.wl, [3], [pos])
+    oc = tiny.ocache()
+    want, oam, _ = oracle.decode_step(tiny.om, oc, [3], [pos])
+    logits_close(got, want)
+    assert list(am) == list(oam)
+
+
+def test_device_errors(tiny):
+    wl = tiny.wl
+    er = _er()
+    for tok, pos, bit in ((wl.shape.vocab, 16, 1), (-1, 16, 1), (5, wl.capacity, 2), (5, -3, 2)):
+        _step(tiny.state, wl, [tok], [pos])
+        st, code, nf = tiny.state.device_error()
+        assert st == er.ER_EDEVICE and code & bit, (tok, pos, code)
+    st, code, nf = tiny.state.device_error()
+    assert st == er.ER_OK and code == 0
+
+
+SMALL_SHAPES = {
+    "q4_tied": synth.ModelShape(**{**TINY.__dict__, "w_type": "q4_0", "tied": True}),
+    "q8_mha": synth.ModelShape(**{**TINY.__dict__, "n_kv_heads": 4}),
+    "q4_hd128_g4": synth.ModelShape(n_layers=2, dim=256, n_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=320,
+                                    vocab=1000, rope_base=500000.0, rms_eps=1e-5, w_type="q4_0", tied=False),
+    "q8_hd64_g3_odd": synth.ModelShape(n_layers=3, dim=96 * 3, n_heads=9, n_kv_heads=3, head_dim=64, ffn_dim=416,
+                                       vocab=777, rope_base=10000.0, rms_eps=1e-6, w_type="q8_0", tied=True),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL_SHAPES))
+@pytest.mark.parametrize("batch", [1, 3, 6])
+def test_small_models_ragged_batch(name, batch):
+    """Tied/untied, Q4_0/Q8_0, G = 1/3/4, hd 64/128, odd sizes; sequences at different positions."""
+    shape = SMALL_SHAPES[name]
+    wl = synth.Workload("t", shape, batch=batch, steps=3, prefill=37)
+    s = Setup(wl)
+    try:
+        rng = np.random.default_rng(batch)
+        tokens = rng.integers(0, shape.vocab, batch)
+        positions = np.array([37, 0, 5, 36, 12, 37][:batch])
+        dev = s.model.device
+        t = torch.tensor(tokens, dtype=torch.int32, device=dev)
+        p = torch.tensor(positions, dtype=torch.int32, device=dev)
+        fed, hist = gpu_chain(s.state, wl, 3, tokens0=tokens, positions0=positions)
+        ofed, ohist = oracle.greedy(s.om, s.ocache(), tokens, positions, 3)
+        np.testing.assert_array_equal(fed, ofed)
+        for st in range(3):
+            logits_close(hist[st], ohist[st])
+        del t, p
+    finally:
+        s.close()
+
+
+def test_nonfinite_flag():
+    """An infinite block scale in the head makes logits non-finite: flag set, argmax stays in range."""
+    shape = SMALL_SHAPES["q8_mha"]
+    weights = synth.gen.model_weights(shape)
+    head = weights["output.weight"].copy()
+    blk = head.reshape(shape.vocab, -1, 34)
+    blk[5, 0, 0:2] = np.frombuffer(np.float16(np.inf).tobytes(), np.uint8)
+    weights["output.weight"] = head
+    wl = synth.Workload("t", shape, batch=1, steps=1, prefill=4)
+    model = gpu_model(shape, weights)
+    st = gpu_state(model, wl)
+    try:
+        got, am = _step(st, wl, [1], [4])
+        status, code, nf = st.device_error()
+        assert nf == 1 and code == 0
+        assert 0 <= am[0] < shape.vocab
+    finally:
+        st.close()
+        model.close()
+
+
+def test_bad_config_rejected():
+    er = _er()
+    from block_quantized_token_gb300 import runtime
+    shape = SMALL_SHAPES["q8_mha"]
+    for field, val, status in (("head_dim", 96, er.ER_EUNSUPPORTED), ("n_kv_heads", 3, er.ER_EINVAL),
+                               ("max_batch", 17, er.ER_EINVAL), ("dim", 48, er.ER_EINVAL)):
+        cfg = runtime.make_config(shape)
+        setattr(cfg, field, val)
+        w = er.er_weights()
+        with pytest.raises(er.ErError) as e:
+            er.er_model_create(cfg, w, 0)
+        assert e.value.status == status, (field, e.value)
+
+
+# ------------------------------------------------------------------------------------------
+# the pages' workload shapes
+# ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["smollm_q8", "smollm_q4"])
+def test_smollm_chain_64(name):
+    """SmolLM2-135M shape, 64 chained greedy steps (context 2048 for Q8_0, 16 for Q4_0)."""
+    wl = synth.workload(name)
+    s = Setup(wl)
+    try:
+        fed, hist = gpu_chain(s.state, wl, wl.steps)
+        ofed, ohist = oracle.greedy(s.om, s.ocache(), wl.tokens0(), wl.positions0(), wl.steps)
+        for st in range(wl.steps):
+            assert fed[st, 0] == ofed[st, 0], f"step {st}: token {fed[st, 0]} vs {ofed[st, 0]}, " \
+                                              f"top-2 gap {top2_gap(ohist[st - 1, 0]):.3e}"
+            logits_close(hist[st], ohist[st])
+    finally:
+        s.close()
