@@ -1,9 +1,10 @@
 """GPU parity of the whole decode step (C ABI) against the float64 oracle.
 
 Gates: logits max |err| <= 2e-3 and relative L2 <= 1e-4 per step; greedy tokens
-identical over the chained steps; appended K/V rows within 1 fp16 ulp (the two
-sides round fp32 / float64 values of k and v to fp16, so a value on a rounding
-boundary may land on either neighbour).
+identical over the chained steps; appended K/V rows within 1 fp16 ulp plus
+1e-5 of the row's largest magnitude (the two sides round fp32 / float64 values
+of k and v to fp16, so a value on a rounding boundary may land on either
+neighbour, and an element near zero carries the fp32 sum's absolute error).
 """
 
 from __future__ import annotations
@@ -13,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import (TINY, gpu_chain, gpu_model, gpu_state, logits_close, oracle_cache, oracle_config,
+from helpers import (gpu_chain, gpu_model, gpu_state, logits_close, oracle_cache, oracle_config,
                      oracle_model, top2_gap)
 
 pytestmark = pytest.mark.gpu
@@ -37,11 +38,14 @@ class Setup:
         return oracle_cache(self.wl, seqs)
 
     def reset_kv(self):
-        """Rewrite the prefill rows (tests that step at low positions overwrite them)."""
-        for b in range(self.wl.batch):
-            for l in range(self.wl.shape.n_layers):
-                k, v = synth.kv_prefill(self.wl, b, l)
+        """Rewrite the prefill rows and zero the rest, as a fresh oracle cache holds them."""
+        wl = self.wl
+        zeros = np.zeros((wl.capacity - wl.prefill, wl.shape.kvd), np.float16)
+        for b in range(wl.batch):
+            for l in range(wl.shape.n_layers):
+                k, v = synth.kv_prefill(wl, b, l)
                 self.state.write_rows(b, l, k, v)
+                self.state.write_rows(b, l, zeros, zeros, start=wl.prefill)
 
     def close(self):
         self.state.close()
@@ -84,7 +88,9 @@ def test_tiny_single_step(tiny):
         for g, w in ((k, ok), (v, ov)):
             g = g.cpu().numpy().reshape(-1).astype(np.float32)
             ulp = np.abs(np.spacing(w.astype(np.float16)).astype(np.float32))
-            assert (np.abs(g - w) <= ulp).all()
+            tol = ulp + 1e-5 * np.abs(w).max()
+            d = np.abs(g - w)
+            assert (d <= tol).all(), f"layer {l}: worst {d.max():.3e} at {d.argmax()} (tol {tol[d.argmax()]:.3e})"
     st, code, nf = tiny.state.device_error()
     assert code == 0 and nf == 0
 
@@ -132,8 +138,10 @@ def test_device_errors(tiny):
 
 
 SMALL_SHAPES = {
-    "q4_tied": synth.ModelShape(**{**TINY.__dict__, "w_type": "q4_0", "tied": True}),
-    "q8_mha": synth.ModelShape(**{**TINY.__dict__, "n_kv_heads": 4}),
+    "q4_tied_g2": synth.ModelShape(n_layers=2, dim=128, n_heads=2, n_kv_heads=1, head_dim=64, ffn_dim=160,
+                                   vocab=300, rope_base=10000.0, rms_eps=1e-5, w_type="q4_0", tied=True),
+    "q8_mha": synth.ModelShape(n_layers=2, dim=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=256, vocab=512,
+                               rope_base=10000.0, rms_eps=1e-5, w_type="q8_0", tied=False),
     "q4_hd128_g4": synth.ModelShape(n_layers=2, dim=256, n_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=320,
                                     vocab=1000, rope_base=500000.0, rms_eps=1e-5, w_type="q4_0", tied=False),
     "q8_hd64_g3_odd": synth.ModelShape(n_layers=3, dim=96 * 3, n_heads=9, n_kv_heads=3, head_dim=64, ffn_dim=416,
