@@ -91,6 +91,7 @@ struct AttnArgs {
 };
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl);
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH);
+cudaError_t attention_prepare();  // kernel attributes (called by gemv_prepare)
 
 // ---------------------------------------------------------------------------
 // small kernels
