@@ -350,12 +350,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the layer count (smaller cases for profiling; not a bench workload)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     wl = synth.workload(args.workload)
+    if args.layers:
+        import dataclasses
+        wl = wl.with_(name=f"{wl.name}_L{args.layers}", shape=dataclasses.replace(wl.shape, n_layers=args.layers))
+        synth.WORKLOADS[wl.name] = wl
+        args.workload = wl.name
     cores = os.cpu_count()
 
     if args.impl == "reference":

@@ -274,6 +274,29 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
             }
         e = cudaMemcpy(kv->rope, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice);
     }
+    // persistent step: layer table, attention partial states, grid barrier
+    {
+        const int max_k = D > qd ? (D > F ? D : F) : (qd > F ? qd : F);
+        kv->step_ok = e == cudaSuccess && step_supported(c.w_type, hd, G, batch, max_k, m->num_sms);
+        kv->schedule = kv->step_ok ? ER_SCHEDULE_PERSISTENT : ER_SCHEDULE_KERNELS;
+        A(&kv->step_layers, (size_t)c.n_layers * sizeof(StepLayer), false);
+        A(&kv->step_apart, step_apart_floats(m->num_sms, hd) * sizeof(float), false);
+        A(&kv->step_acnt, (size_t)batch * c.n_kv_heads * sizeof(int));
+        A(&kv->step_bar, sizeof(unsigned));
+        if (e == cudaSuccess) {
+            std::vector<StepLayer> ls(c.n_layers);
+            for (int l = 0; l < c.n_layers; ++l) {
+                const er_layer_dev &L = m->layers[l];
+                ls[l].w[0] = L.qkv.d;
+                ls[l].w[1] = L.wo.d;
+                ls[l].w[2] = L.gateup.d;
+                ls[l].w[3] = L.down.d;
+                ls[l].attn_norm = L.attn_norm;
+                ls[l].ffn_norm = L.ffn_norm;
+            }
+            e = cudaMemcpy(kv->step_layers, ls.data(), ls.size() * sizeof(StepLayer), cudaMemcpyHostToDevice);
+        }
+    }
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&kv->cap_stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -464,8 +487,59 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
     return cudaErrorInvalidValue;
 }
 
+static cudaError_t enqueue_persistent(er_kv *kv, const int32_t *tokens, const int32_t *positions, float *logits,
+                                      int32_t *argmax, cudaStream_t st) {
+    er_model *m = kv->m;
+    const er_config &c = m->cfg;
+    StepArgs a = {};
+    a.layers = kv->step_layers;
+    a.head = m->head.d;
+    a.out_norm = m->out_norm;
+    a.embd_f16 = c.tied ? nullptr : m->embd_f16;
+    a.L = c.n_layers;
+    a.D = c.dim;
+    a.H = c.n_heads;
+    a.KV = c.n_kv_heads;
+    a.hd = c.head_dim;
+    a.F = c.ffn_dim;
+    a.V = c.vocab;
+    a.qd = c.n_heads * c.head_dim;
+    a.kvd = c.n_kv_heads * c.head_dim;
+    a.B = kv->B;
+    a.cap = kv->cap;
+    const er::Mat *mats[5] = {&m->layers[0].qkv, &m->layers[0].wo, &m->layers[0].gateup, &m->layers[0].down, &m->head};
+    for (int i = 0; i < 5; ++i) {
+        a.R[i] = mats[i]->R;
+        a.UPR[i] = mats[i]->UPR;
+    }
+    a.eps = (float)c.rms_eps;
+    a.tokens = tokens;
+    a.positions = positions;
+    a.x = kv->x;
+    a.q = kv->q;
+    a.o = kv->o;
+    a.a = kv->a;
+    a.kc = kv->kc;
+    a.vc = kv->vc;
+    a.rope = kv->rope;
+    a.logits = logits;
+    a.argmax = argmax;
+    a.part = kv->gemv_part;
+    a.cnt = kv->gemv_cnt;
+    a.apart = kv->step_apart;
+    a.acnt = kv->step_acnt;
+    a.amax = kv->amax;
+    a.done = kv->done;
+    a.flags = kv->flags;
+    a.bar = kv->step_bar;
+    cudaError_t e = cudaMemsetAsync(kv->step_bar, 0, sizeof(unsigned), st);
+    if (e == cudaSuccess) e = launch_step(c.w_type, a, m->num_sms, st);
+    return e;
+}
+
 static cudaError_t enqueue_step(er_kv *kv, const int32_t *tokens, const int32_t *positions, float *logits,
                                 int32_t *argmax, cudaStream_t st, bool pdl) {
+    if (kv->schedule == ER_SCHEDULE_PERSISTENT) return enqueue_persistent(kv, tokens, positions, logits, argmax, st);
     cudaError_t e = enqueue_stage(kv, ER_STAGE_EMBED, 0, tokens, positions, logits, argmax, st, pdl);
     for (int l = 0; l < kv->m->cfg.n_layers && e == cudaSuccess; ++l)
         for (int s = ER_STAGE_QKV; s <= ER_STAGE_DOWN && e == cudaSuccess; ++s)
@@ -526,6 +600,29 @@ er_status er_launch_stage(er_kv *kv, int32_t stage, int32_t layer, const int32_t
     ER_CUDA(enqueue_stage(kv, stage, layer, tokens, positions, logits, argmax, (cudaStream_t)stream, false));
     return ER_OK;
 }
+
+er_status er_kv_set_schedule(er_kv *kv, int32_t schedule) {
+    if (!kv) return fail(ER_EINVAL, "kv is NULL");
+    int want;
+    switch (schedule) {
+        case ER_SCHEDULE_AUTO: want = kv->step_ok ? ER_SCHEDULE_PERSISTENT : ER_SCHEDULE_KERNELS; break;
+        case ER_SCHEDULE_PERSISTENT:
+            if (!kv->step_ok) return fail(ER_EUNSUPPORTED, "the persistent step cannot run this shape");
+            want = ER_SCHEDULE_PERSISTENT;
+            break;
+        case ER_SCHEDULE_KERNELS: want = ER_SCHEDULE_KERNELS; break;
+        default: return fail(ER_EINVAL, "bad schedule");
+    }
+    if (want != kv->schedule) {
+        ER_CUDA(cudaDeviceSynchronize());
+        for (auto &g : kv->graphs) cudaGraphExecDestroy(g.exec);
+        kv->graphs.clear();
+        kv->schedule = want;
+    }
+    return ER_OK;
+}
+
+int32_t er_kv_get_schedule(const er_kv *kv) { return kv ? kv->schedule : -1; }
 
 er_status er_positions_increment(int32_t *positions, int32_t batch, void *stream) {
     if (!positions || batch < 1) return fail(ER_EINVAL, "bad positions/batch");

@@ -46,15 +46,17 @@ ER_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-// Returns true once the phase with parity `parity` has completed.
+// Returns true once the phase with parity `parity` has completed; a thread may
+// be suspended for up to about 20 us inside the call while it waits (rather
+// than spinning and taking issue slots from the warps that compute).
 ER_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(20000)
         : "memory");
     return ok != 0;
 }
@@ -64,6 +66,15 @@ ER_DEV int atom_add_acq_rel_gpu(int *p, int v) {
     int old;
     asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+ER_DEV void red_add_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+ER_DEV unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 ER_DEV uint64_t globaltimer_ns() {

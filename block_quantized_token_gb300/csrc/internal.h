@@ -94,6 +94,44 @@ void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH
 cudaError_t attention_prepare();  // kernel attributes (called by gemv_prepare)
 
 // ---------------------------------------------------------------------------
+// persistent decode step (kernels_step.cuh)
+// ---------------------------------------------------------------------------
+#define ER_MK_MAXB 4
+#define ER_MK_MAXG 4
+struct StepLayer {
+    const uint8_t *w[4];  // repacked QKV (PAIR), Wo, gate/up (GATEUP), down
+    const float *attn_norm, *ffn_norm;
+};
+struct StepArgs {
+    const StepLayer *layers;  // device array [L]
+    const uint8_t *head;      // repacked head (tied: token_embd)
+    const float *out_norm;
+    const __half *embd_f16;   // untied embedding, or nullptr
+    int L, D, H, KV, hd, F, V, qd, kvd, B, cap;
+    int R[5], UPR[5];         // row groups / units per row group: QKV, WO, GATEUP, DOWN, HEAD
+    float eps;
+    const int32_t *tokens, *positions;
+    float *x, *q, *o, *a;
+    __half *kc, *vc;
+    const float2 *rope;
+    float *logits;
+    int32_t *argmax;
+    float *part;    // GEMV cross-CTA partials
+    int *cnt;       // GEMV cross-CTA counters
+    float *apart;   // attention partial states [warps][2][G][hd + 2]
+    int *acnt;      // attention counters [B * KV]
+    unsigned long long *amax;
+    int *done, *flags;
+    unsigned *bar;  // grid barrier counter (zeroed before each launch)
+};
+// Whether the persistent step can run this shape (batch, GQA group, head dim,
+// shared memory) and the launch itself (cooperative, one CTA per SM).
+bool step_supported(int qt, int hd, int G, int B, int max_k, int num_sms);
+cudaError_t launch_step(int qt, const StepArgs &a, int num_sms, cudaStream_t st);
+size_t step_apart_floats(int num_sms, int hd);
+cudaError_t step_prepare();
+
+// ---------------------------------------------------------------------------
 // small kernels
 // ---------------------------------------------------------------------------
 struct EmbedArgs {
@@ -146,6 +184,12 @@ struct er_graph_entry {
 struct er_kv {
     er_model *m;
     int B, cap, S, CH;
+    int schedule;        // ER_SCHEDULE_PERSISTENT or ER_SCHEDULE_KERNELS (resolved)
+    bool step_ok;        // the persistent step supports this shape
+    er::StepLayer *step_layers;
+    float *step_apart;
+    int *step_acnt;
+    unsigned *step_bar;
     __half *kc, *vc;
     float2 *rope;
     float *x, *q, *o, *a;

@@ -1,8 +1,6 @@
 // Create-time repack of GGUF blocks, the dequantisation test kernel, the
 // embedding gather and the position increment.
-#include "common.cuh"
-#include "internal.h"
-#include "layout.cuh"
+#include "gemv_core.cuh"
 
 namespace er {
 
@@ -85,31 +83,6 @@ cudaError_t launch_repack(const Mat &m, const RepackSrc &src, cudaStream_t st) {
     if (blocks > 65535u * 16) blocks = 65535u * 16;
     repack_kernel<<<(unsigned)blocks, threads, 0, st>>>(m.d, src, m.qt, m.rowmap, m.K, m.UPR, total);
     return cudaGetLastError();
-}
-
-// Value of element (row, col) of an IDENT-mapped repacked matrix, decoded with
-// the same register conversions the GEMV uses.
-__device__ inline float repacked_value(const uint8_t *W, int qt, int UPR, int row, int col) {
-    int rg = row >> 4, r = row & 15;
-    int unit = col >> 6, c = col & 63;
-    const uint8_t *ub = W + ((size_t)rg * UPR + unit) * unit_bytes_of(qt);
-    FragPos p = frag_pos(r, c);
-    __half dh = *reinterpret_cast<const __half *>(ub + scale_offset(qt, r, p.b));
-    uint32_t h2;
-    if (qt == Q8_0) {
-        int off = q8_byte_offset(p);
-        uint32_t w = *reinterpret_cast<const uint32_t *>(ub + (off & ~3));
-        uint32_t lo, hi;
-        q8_word_to_h2(w, lo, hi);
-        h2 = (off & 2) ? hi : lo;
-        return __half2float(dh) * ((off & 1) ? h2f_hi(h2) : h2f_lo(h2));
-    }
-    int word = 2 * p.b + p.h;
-    uint32_t w = *reinterpret_cast<const uint32_t *>(ub + p.lane * 16 + word * 4);
-    uint32_t rr[4];
-    q4_word_to_h2(w, rr);
-    h2 = rr[p.reg];
-    return __half2float(dh) * (p.e ? h2f_hi(h2) : h2f_lo(h2));
 }
 
 __global__ void dequant_kernel(const uint8_t *__restrict__ W, int qt, int UPR, int N, int K, float *__restrict__ out) {

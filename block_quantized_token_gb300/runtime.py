@@ -107,6 +107,13 @@ class DecodeState:
         fn(tokens.data_ptr(), positions.data_ptr(), self.handle, None if logits is None else logits.data_ptr(),
            None if argmax is None else argmax.data_ptr(), st)
 
+    def set_schedule(self, schedule: int) -> None:
+        er.er_kv_set_schedule(self.handle, schedule)
+
+    @property
+    def schedule(self) -> int:
+        return er.er_kv_get_schedule(self.handle)
+
     def device_error(self) -> tuple[int, int, int]:
         return er.er_get_device_error(self.handle)
 

@@ -150,6 +150,20 @@ ER_API er_status er_decode_step(const int32_t *tokens_dev, const int32_t *positi
 ER_API er_status er_decode_step_eager(const int32_t *tokens_dev, const int32_t *positions_dev, er_kv *kv,
                                float *logits_dev, int32_t *argmax_dev, void *stream);
 
+/* How er_decode_step runs the step:
+ *   ER_SCHEDULE_AUTO        persistent when the shape allows it (default)
+ *   ER_SCHEDULE_PERSISTENT  one cooperative kernel, one CTA per SM, that runs
+ *                           every phase with grid barriers in between and
+ *                           streams weights continuously (batch <= 4,
+ *                           n_heads / n_kv_heads <= 4, shared memory permitting)
+ *   ER_SCHEDULE_KERNELS     one kernel per phase (any supported shape)
+ * Both compute the same step; the choice drops kv's recorded graphs.
+ * ER_EUNSUPPORTED if PERSISTENT is asked for a shape it cannot run. */
+typedef enum { ER_SCHEDULE_AUTO = 0, ER_SCHEDULE_PERSISTENT = 1, ER_SCHEDULE_KERNELS = 2 } er_schedule;
+ER_API er_status er_kv_set_schedule(er_kv *kv, int32_t schedule);
+/* The schedule in effect (ER_SCHEDULE_PERSISTENT or ER_SCHEDULE_KERNELS), or -1 for NULL. */
+ER_API int32_t er_kv_get_schedule(const er_kv *kv);
+
 /* positions_dev[b] += 1 for b < batch (chains steps without a host round trip). */
 ER_API er_status er_positions_increment(int32_t *positions_dev, int32_t batch, void *stream);
 
@@ -161,8 +175,9 @@ ER_API er_status er_positions_increment(int32_t *positions_dev, int32_t batch, v
  * Returns ER_EDEVICE if *code != 0, else ER_OK. */
 ER_API er_status er_get_device_error(er_kv *kv, int32_t *code, int32_t *non_finite);
 
-/* Stage kernels of the step, queued alone with the step's own arguments for
- * layer `layer` (ignored by EMBED and HEAD).  For per-kernel timing. */
+/* Stage kernels of the per-phase schedule (ER_SCHEDULE_KERNELS), queued alone
+ * with the step's own arguments for layer `layer` (ignored by EMBED and HEAD).
+ * For per-kernel timing. */
 typedef enum {
     ER_STAGE_EMBED = 0,   /* token row -> residual x                          */
     ER_STAGE_QKV = 1,     /* RMSNorm + [Wq;Wk;Wv] + RoPE + K/V append          */

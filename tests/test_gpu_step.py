@@ -26,12 +26,17 @@ def _er():
     return er
 
 
+PERSISTENT, KERNELS = 1, 2  # er_schedule values
+
+
 class Setup:
-    def __init__(self, wl, max_batch=None, seqs=None):
+    def __init__(self, wl, max_batch=None, seqs=None, schedule=None):
         self.wl = wl
         self.weights = synth.gen.model_weights(wl.shape)
         self.model = gpu_model(wl.shape, self.weights, max_batch=max_batch or wl.batch)
         self.state = gpu_state(self.model, wl)
+        if schedule is not None:
+            self.state.set_schedule(schedule)
         self.om = oracle_model(wl.shape, self.weights)
 
     def ocache(self, seqs=None):
@@ -95,6 +100,24 @@ def test_tiny_single_step(tiny):
     assert code == 0 and nf == 0
 
 
+def test_schedules_agree(tiny):
+    """The persistent step and the per-phase kernels compute the same step."""
+    wl = tiny.wl
+    assert tiny.state.schedule == PERSISTENT  # chosen automatically for this shape
+    tiny.reset_kv()
+    a, am_a = _step(tiny.state, wl, wl.tokens0(), wl.positions0())
+    tiny.state.set_schedule(KERNELS)
+    try:
+        b, am_b = _step(tiny.state, wl, wl.tokens0(), wl.positions0())
+    finally:
+        tiny.state.set_schedule(PERSISTENT)
+    want, oam, _ = oracle.decode_step(tiny.om, tiny.ocache(), wl.tokens0(), wl.positions0())
+    logits_close(a, want)
+    logits_close(b, want)
+    assert list(am_a) == list(am_b) == list(oam)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-4)
+
+
 def test_graph_equals_eager_and_deterministic(tiny):
     wl = tiny.wl
     a, am_a = _step(tiny.state, wl, wl.tokens0(), wl.positions0(), graph=True)
@@ -149,13 +172,24 @@ SMALL_SHAPES = {
 }
 
 
+@pytest.mark.parametrize("schedule", [PERSISTENT, KERNELS], ids=["persistent", "kernels"])
 @pytest.mark.parametrize("name", list(SMALL_SHAPES))
 @pytest.mark.parametrize("batch", [1, 3, 6])
-def test_small_models_ragged_batch(name, batch):
+def test_small_models_ragged_batch(name, batch, schedule):
     """Tied/untied, Q4_0/Q8_0, G = 1/3/4, hd 64/128, odd sizes; sequences at different positions."""
     shape = SMALL_SHAPES[name]
     wl = synth.Workload("t", shape, batch=batch, steps=3, prefill=37)
-    s = Setup(wl)
+    if schedule == PERSISTENT and batch > 4:
+        s = Setup(wl)
+        try:
+            with pytest.raises(_er().ErError) as e:
+                s.state.set_schedule(PERSISTENT)
+            assert e.value.status == _er().ER_EUNSUPPORTED
+            assert s.state.schedule == KERNELS
+        finally:
+            s.close()
+        return
+    s = Setup(wl, schedule=schedule)
     try:
         rng = np.random.default_rng(batch)
         tokens = rng.integers(0, shape.vocab, batch)
@@ -211,11 +245,12 @@ def test_bad_config_rejected():
 # ------------------------------------------------------------------------------------------
 # the pages' workload shapes
 # ------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("schedule", [PERSISTENT, KERNELS], ids=["persistent", "kernels"])
 @pytest.mark.parametrize("name", ["smollm_q8", "smollm_q4"])
-def test_smollm_chain_64(name):
+def test_smollm_chain_64(name, schedule):
     """SmolLM2-135M shape, 64 chained greedy steps (context 2048 for Q8_0, 16 for Q4_0)."""
     wl = synth.workload(name)
-    s = Setup(wl)
+    s = Setup(wl, schedule=schedule)
     try:
         fed, hist = gpu_chain(s.state, wl, wl.steps)
         ofed, ohist = oracle.greedy(s.om, s.ocache(), wl.tokens0(), wl.positions0(), wl.steps)
