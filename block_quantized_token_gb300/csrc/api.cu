@@ -79,6 +79,10 @@ int device_sms(int *dev) {
 
 }  // namespace
 
+// error reporting for entry points defined in other files
+er_status er_fail_status(er_status s, const char *msg) { return fail(s, "%s", msg); }
+er_status er_fail_cuda(cudaError_t e, const char *what) { return cuda_fail(e, what); }
+
 extern "C" {
 
 const char *er_status_str(er_status s) {

@@ -147,6 +147,10 @@ cudaError_t launch_positions_increment(int32_t *pos, int n, cudaStream_t st);
 
 }  // namespace er
 
+// error reporting shared by the entry points (sets er_last_error)
+er_status er_fail_status(er_status s, const char *msg);
+er_status er_fail_cuda(cudaError_t e, const char *what);
+
 // ---------------------------------------------------------------------------
 // opaque API objects
 // ---------------------------------------------------------------------------

@@ -5,6 +5,8 @@
 // copies (cp.async.bulk, completion on an mbarrier).  The first slots are
 // requested before griddepcontrol.wait, so the weight traffic of this kernel
 // overlaps the tail of the previous one.
+#include <mutex>
+
 #include "gemv_core.cuh"
 
 namespace er {
@@ -163,3 +165,78 @@ cudaError_t launch_gemv(int epi, const GemvArgs &a, int num_sms, cudaStream_t st
 }
 
 }  // namespace er
+
+// ---------------------------------------------------------------------------
+// er_matrix_gemv_noalloc: the stand-alone GEMV with its scratch in a fixed array
+// ---------------------------------------------------------------------------
+namespace er {
+
+// Scratch of the allocation-free GEMV, compiled into the library (every GPU that
+// loads the library holds it until the process exits):
+//   [partials: NOALLOC_MAX_SMS * 2 * 64 floats][counters: NOALLOC_MAX_RG ints][flag: 64 ints]
+constexpr int NOALLOC_MAX_SMS = 256;
+constexpr int NOALLOC_MAX_RG = 16384;  // row groups of 16 rows: up to 262144 rows
+constexpr size_t NOALLOC_PART_BYTES = (size_t)NOALLOC_MAX_SMS * 2 * 64 * sizeof(float);
+constexpr size_t NOALLOC_CNT_BYTES = (size_t)NOALLOC_MAX_RG * sizeof(int);
+constexpr size_t NOALLOC_BYTES = NOALLOC_PART_BYTES + NOALLOC_CNT_BYTES + 64 * sizeof(int);
+
+static __device__ __align__(256) unsigned char noalloc_scratch[NOALLOC_BYTES];
+
+// Device address of noalloc_scratch on each device, looked up once per device
+// (with that device current) on the first call there.  The name of the array
+// in host code is only a host-side stand-in, so kernels get this address.
+static unsigned char *noalloc_addr[64];
+static std::mutex noalloc_mutex;
+
+static cudaError_t noalloc_scratch_for(int device, unsigned char **out) {
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(noalloc_mutex);
+    if (!noalloc_addr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        noalloc_addr[device] = static_cast<unsigned char *>(p);
+    }
+    *out = noalloc_addr[device];
+    return cudaSuccess;
+}
+
+}  // namespace er
+
+extern "C" er_status er_matrix_gemv_noalloc(const er_matrix *x, const float *xin, int32_t batch, float *y,
+                                           void *stream) {
+    using namespace er;
+    if (!x || !xin || !y) return er_fail_status(ER_EINVAL, "NULL argument");
+    if (batch < 1 || batch > 16) return er_fail_status(ER_EINVAL, "batch must be in 1..16");
+    if (x->m.R > NOALLOC_MAX_RG) return er_fail_status(ER_EINVAL, "matrix has more rows than the fixed scratch holds");
+    if (x->num_sms > NOALLOC_MAX_SMS) return er_fail_status(ER_EUNSUPPORTED, "more SMs than the fixed scratch holds");
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    unsigned char *base = nullptr;
+    if (e == cudaSuccess) e = noalloc_scratch_for(device, &base);
+    if (e != cudaSuccess) return er_fail_cuda(e, "er_matrix_gemv_noalloc set-up");
+    cudaStream_t st = (cudaStream_t)stream;
+    GemvArgs a = {};
+    a.W = x->m.d;
+    a.R = x->m.R;
+    a.UPR = x->m.UPR;
+    a.N = x->m.N;
+    a.K = x->m.K;
+    a.qt = x->m.qt;
+    a.x = xin;
+    a.y = y;
+    a.part = reinterpret_cast<float *>(base);
+    a.cnt = reinterpret_cast<int *>(base + NOALLOC_PART_BYTES);
+    a.flags = reinterpret_cast<int *>(base + NOALLOC_PART_BYTES + NOALLOC_CNT_BYTES);
+    // the array keeps the last call's contents: counters and the flag start at zero
+    e = cudaMemsetAsync(a.cnt, 0, (size_t)a.R * sizeof(int), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.flags, 0, sizeof(int), st);
+    const int per = gemv_max_cols(a.qt, a.K);
+    for (int b0 = 0; b0 < batch && e == cudaSuccess; b0 += per) {
+        a.b0 = b0;
+        a.B = batch - b0 < per ? batch - b0 : per;
+        e = launch_gemv(EPI_STORE, a, x->num_sms, st, false);
+    }
+    if (e != cudaSuccess) return er_fail_cuda(e, "er_matrix_gemv_noalloc");
+    return ER_OK;
+}

@@ -71,6 +71,7 @@ def _load() -> ctypes.CDLL:
         "er_matrix_destroy": (None, [VP]),
         "er_matrix_dequant": (I32, [VP, VP, VP]),
         "er_matrix_gemv": (I32, [VP, VP, I32, VP, VP]),
+        "er_matrix_gemv_noalloc": (I32, [VP, VP, I32, VP, VP]),
         "er_status_str": (ctypes.c_char_p, [I32]),
         "er_last_error": (ctypes.c_char_p, []),
     }
@@ -86,7 +87,7 @@ EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_
             "er_kv_layer_ptrs", "er_kv_write", "er_kv_read", "er_decode_step", "er_decode_step_eager", "er_positions_increment",
             "er_kv_set_schedule", "er_kv_get_schedule",
             "er_get_device_error", "er_launch_stage", "er_matrix_create", "er_matrix_destroy",
-            "er_matrix_dequant", "er_matrix_gemv", "er_status_str", "er_last_error")
+            "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_status_str", "er_last_error")
 
 
 def lib() -> ctypes.CDLL:
@@ -199,3 +200,7 @@ def er_matrix_dequant(mat: int, out: int, stream: int = 0) -> None:
 
 def er_matrix_gemv(mat: int, x: int, batch: int, y: int, stream: int = 0) -> None:
     _check(_lib.er_matrix_gemv(mat, x, batch, y, stream), "er_matrix_gemv")
+
+
+def er_matrix_gemv_noalloc(mat: int, x: int, batch: int, y: int, stream: int = 0) -> None:
+    _check(_lib.er_matrix_gemv_noalloc(mat, x, batch, y, stream), "er_matrix_gemv_noalloc")

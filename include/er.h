@@ -205,6 +205,26 @@ ER_API er_status er_matrix_dequant(const er_matrix *mat, float *out_dev, void *s
  * rows).  fp32 activations, fp32 accumulation; deterministic. */
 ER_API er_status er_matrix_gemv(const er_matrix *mat, const float *x_dev, int32_t batch, float *y_dev, void *stream);
 
+/* The product of er_matrix_gemv for callers that cannot allocate device
+ * memory when they run it (a process whose device memory is all handed out by
+ * its own pool, code that must not call cudaMalloc while other threads capture
+ * CUDA graphs, ...).  The weights are read from `mat`; x_dev and y_dev are the
+ * caller's, as for er_matrix_gemv.  The partial sums and counters that
+ * er_matrix_gemv keeps in buffers er_matrix_create allocated live here in one
+ * array compiled into the library instead: 192.25 KiB per GPU, held by every
+ * GPU that loads the library until the process exits.  No cudaMalloc, cudaFree
+ * or allocating library call is made.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the array and it keeps the last call's contents; the
+ *     call clears the part that must start at zero.  Calls that overlap on the
+ *     GPU (other streams, other threads) race on it: serialise them.
+ *   - Limits: at most 262144 rows (16384 row groups) and 256 SMs; larger
+ *     matrices give ER_EINVAL, more SMs ER_EUNSUPPORTED.
+ * There is no counterpart on the pages; it exists for this library's callers. */
+ER_API er_status er_matrix_gemv_noalloc(const er_matrix *mat, const float *x_dev, int32_t batch, float *y_dev,
+                                        void *stream);
+
 ER_API const char *er_status_str(er_status s);
 ER_API const char *er_last_error(void);
 
