@@ -149,6 +149,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             state.write_rows(b, l, k, v)
     setup_s = time.time() - t0
 
+    if args.schedule != "auto":
+        state.set_schedule({"persistent": er.ER_SCHEDULE_PERSISTENT, "kernels": er.ER_SCHEDULE_KERNELS}[args.schedule])
+    schedule = {er.ER_SCHEDULE_PERSISTENT: "persistent", er.ER_SCHEDULE_KERNELS: "kernels"}[state.schedule]
+    launches_step = er.er_kv_launches_per_step(state.handle)
+
     stream = torch.cuda.Stream(dev)
     sp = stream.cuda_stream
     tok = torch.empty(B, dtype=torch.int32, device=dev)
@@ -177,14 +182,21 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     clocks = ClockSampler(local_rank)
     if rank == 0:
         clocks.start()
+    # events around every step graph (on the launching stream) give the step
+    # kernel's own duration; the outer pair times the whole chain
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     ev0.record(stream)
-    for _ in range(K):
-        one_step()
+    for i in range(K):
+        evs[i][0].record(stream)
+        er.er_decode_step(tok.data_ptr(), pos.data_ptr(), state.handle, logits.data_ptr(), tok.data_ptr(), sp)
+        evs[i][1].record(stream)
+        er.er_positions_increment(pos.data_ptr(), B, sp)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     ms = ev0.elapsed_time(ev1)
+    graph_ms = [a.elapsed_time(b) for a, b in evs]
     clock_info = clocks.stop() if rank == 0 else None
     if dist is not None:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -224,16 +236,27 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
 
-    # ---- per-stage launch durations (eager launches, L2 flushed before each) for the roofline
+    positions = wl.positions0()[None, :] + np.arange(K)[:, None]
+    per_step_bytes = [step_bytes(wl, p) for p in positions]
+    bytes_step = float(np.mean(per_step_bytes))
+
+    # ---- roofline of the dominant kernel
     roof = None
     if rank == 0:
-        roof = stage_roofline(er, state, wl, tok, pos, logits, stream, dev)
+        peaks = measured_peaks()
+        if schedule == "persistent":
+            # one launch per step: the step kernel is the whole step (plus a 4-byte memset in the same graph)
+            launch_ms = float(np.mean(graph_ms))
+            achieved = bytes_step / (launch_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "kernel": "step_kernel", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                    "peak_source": f"{peaks['source']} hbm_gbs (STREAM-style copy)",
+                    "bytes_per_launch": bytes_step, "us_per_launch": launch_ms * 1e3,
+                    "timing": "CUDA events around each step graph inside the timed region"}
+        else:
+            roof = stage_roofline(er, state, wl, tok, pos, logits, stream, dev)
 
-    positions = wl.positions0()[None, :] + np.arange(K)[:, None]
-    bytes_step = float(np.mean([step_bytes(wl, p) for p in positions]))
     tokens = B * K * world
-    gemv_groups = 1 if B <= 4 else (B + 3) // 4  # column groups per GEMV launch set
-    launches = 1 + s.n_layers * (1 + 4 * gemv_groups) + gemv_groups + 1
     result = None
     if rank == 0:
         result = {
@@ -252,13 +275,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "config": {"workload": wl.name, "model": f"{s.n_layers}L d{s.dim} {s.n_heads}/{s.n_kv_heads}x{s.head_dim} "
                                                      f"ffn{s.ffn_dim} V{s.vocab} {s.w_type} "
                                                      f"{'tied' if s.tied else 'untied'}",
-                       "batch": B, "context": wl.prefill, "chained_steps": K,
+                       "batch": B, "context": wl.prefill, "chained_steps": K, "schedule": schedule,
                        "step_bytes": bytes_step, "step_gbs": bytes_step / (ms / K / 1e3) / 1e9,
                        "step_roofline_frac": bytes_step / (ms / K / 1e3) / 1e9 / measured_peaks()["hbm_gbs"],
                        "l2": ("inputs larger than L2" if bytes_step > 129e6 else "L2-resident working set"),
                        "parallelism": f"replicas x{world}", "setup_s": round(setup_s, 1)},
             "e2e": {"value": tokens / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
-            "gpu_launches": launches * K,
+            "gpu_launches": (launches_step + 1) * K,
             "roofline": roof,
             "clocks": clock_info,
         }
@@ -348,6 +371,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="smollm_q8", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--schedule", default="auto", choices=["auto", "persistent", "kernels"],
+                    help="step schedule (auto: the persistent kernel where the shape allows it)")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,

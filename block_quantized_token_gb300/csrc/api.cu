@@ -281,7 +281,15 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
     // persistent step: layer table, attention partial states, grid barrier
     {
         const int max_k = D > qd ? (D > F ? D : F) : (qd > F ? qd : F);
-        kv->step_ok = e == cudaSuccess && step_supported(c.w_type, hd, G, batch, max_k, m->num_sms);
+        const er::Mat *mats[5] = {&m->layers[0].qkv, &m->layers[0].wo, &m->layers[0].gateup, &m->layers[0].down,
+                                  &m->head};
+        int R[5], UPR[5];
+        for (int i = 0; i < 5; ++i) {
+            R[i] = mats[i]->R;
+            UPR[i] = mats[i]->UPR;
+        }
+        kv->step_ok = e == cudaSuccess && step_supported(c.w_type, hd, G, batch, c.n_kv_heads, capacity, max_k, R, UPR,
+                                                         m->num_sms);
         kv->schedule = kv->step_ok ? ER_SCHEDULE_PERSISTENT : ER_SCHEDULE_KERNELS;
         A(&kv->step_layers, (size_t)c.n_layers * sizeof(StepLayer), false);
         A(&kv->step_apart, step_apart_floats(m->num_sms, hd) * sizeof(float), false);
@@ -627,6 +635,20 @@ er_status er_kv_set_schedule(er_kv *kv, int32_t schedule) {
 }
 
 int32_t er_kv_get_schedule(const er_kv *kv) { return kv ? kv->schedule : -1; }
+
+int32_t er_kv_launches_per_step(const er_kv *kv) {
+    if (!kv) return -1;
+    if (kv->schedule == ER_SCHEDULE_PERSISTENT) return 1;
+    const er_model *m = kv->m;
+    const er_config &c = m->cfg;
+    auto groups = [&](const er::Mat &w) {
+        const int per = gemv_max_cols(w.qt, w.K);
+        return per > 0 ? (kv->B + per - 1) / per : 0;
+    };
+    const er_layer_dev &L0 = m->layers[0];
+    const int per_layer = groups(L0.qkv) + 1 + groups(L0.wo) + groups(L0.gateup) + groups(L0.down);
+    return 1 + c.n_layers * per_layer + groups(m->head);
+}
 
 er_status er_positions_increment(int32_t *positions, int32_t batch, void *stream) {
     if (!positions || batch < 1) return fail(ER_EINVAL, "bad positions/batch");

@@ -84,35 +84,45 @@ __device__ inline GvScratch gv_scratch(uint8_t *base) {
 // `aligned`, CTAs take whole row groups (C = min(R, max_ctas) CTAs, R/C or
 // R/C + 1 row groups each): no row group is shared by CTAs, at the price of
 // at most one row group of imbalance.
+// Unit indices are 32-bit: the launchers require R * UPR * max_ctas < 2^31.
 struct GvRange {
-    long long ca, cb, wa, wb;  // CTA range, warp range
-    int n, nw;                 // CTA units, working warps
+    int ca, cb, wa, wb;  // CTA range, warp range
+    int n, nw;           // CTA units, working warps
+    int rgf, j0;         // row group of unit wa, and wa's position in it
     bool cta_active, working;
 };
 
+__host__ __device__ inline bool gv_index_ok(long long R, long long UPR, long long max_ctas) {
+    return R * UPR * (max_ctas + 1) < (1ll << 31);
+}
+
 __device__ inline GvRange gv_range(int R, int UPR, int cta, int max_ctas, int warp, bool aligned = false) {
     GvRange r;
-    const long long U = (long long)R * UPR;
+    const int U = R * UPR;
     const int nC = aligned ? (R < max_ctas ? R : max_ctas) : gv_ctas(R, UPR, max_ctas);
     r.cta_active = cta < nC;
     if (!r.cta_active) {
         r.ca = r.cb = r.wa = r.wb = U;
         r.n = r.nw = 0;
+        r.rgf = R;
+        r.j0 = 0;
         r.working = false;
         return r;
     }
     if (aligned) {
-        r.ca = (long long)cta * R / nC * UPR;
-        r.cb = (long long)(cta + 1) * R / nC * UPR;
+        r.ca = cta * R / nC * UPR;
+        r.cb = (cta + 1) * R / nC * UPR;
     } else {
-        r.ca = (long long)cta * U / nC;
-        r.cb = (long long)(cta + 1) * U / nC;
+        r.ca = (int)((long long)cta * U / nC);
+        r.cb = (int)((long long)(cta + 1) * U / nC);
     }
-    r.n = (int)(r.cb - r.ca);
+    r.n = r.cb - r.ca;
     r.nw = r.n < GV_WARPS ? r.n : GV_WARPS;
     r.working = warp < r.nw;
-    r.wa = r.working ? r.ca + (long long)warp * r.n / r.nw : r.cb;
-    r.wb = r.working ? r.ca + (long long)(warp + 1) * r.n / r.nw : r.cb;
+    r.wa = r.working ? r.ca + warp * r.n / r.nw : r.cb;
+    r.wb = r.working ? r.ca + (warp + 1) * r.n / r.nw : r.cb;
+    r.rgf = r.wa / UPR;
+    r.j0 = r.wa - r.rgf * UPR;
     return r;
 }
 
@@ -161,21 +171,27 @@ __device__ inline void gv_epilogue(const GemvArgs &a, int rg, float v0, float v1
             if (r0 < a.N) y[r0] = v0;
             if (r1 < a.N) y[r1] = v1;
         } else {
-            if (r0 < a.N) y[r0] = __ldcg(y + r0) + v0;
-            if (r1 < a.N) y[r1] = __ldcg(y + r1) + v1;
+            const int lr = rg - a.resid_rg0;
+            if (a.resid_s && lr >= 0 && lr < a.resid_nrg) {  // rows staged at the start of the phase
+                if (r0 < a.N) y[r0] = a.resid_s[(lr * 16 + g) * GV_MAXB + bt] + v0;
+                if (r1 < a.N) y[r1] = a.resid_s[(lr * 16 + g + 8) * GV_MAXB + bt] + v1;
+            } else {
+                if (r0 < a.N) y[r0] = __ldcg(y + r0) + v0;
+                if (r1 < a.N) y[r1] = __ldcg(y + r1) + v1;
+            }
         }
     } else if (EPI == EPI_QKV) {
         if (!bok) return;
         v0 *= f;
         v1 *= f;
-        const int pos = a.positions[bt];
+        const int pos = a.pos_s ? a.pos_s[bt] : a.positions[bt];
         if (pos < 0 || pos >= a.cap) return;
         int r0 = 16 * rg + 2 * g;  // RoPE pair (r0, r0 + 1)
         if (r0 >= a.qd + 2 * a.kvd) return;
         if (r0 < a.qd + a.kvd) {  // q or k: rotate
             int base = r0 < a.qd ? r0 : r0 - a.qd;
             int dd = base % a.hd;
-            float2 cs = a.rope[(size_t)pos * (a.hd / 2) + dd / 2];
+            const float2 cs = a.rope_s ? a.rope_s[bt * (a.hd / 2) + dd / 2] : a.rope[(size_t)pos * (a.hd / 2) + dd / 2];
             float o0 = v0 * cs.x - v1 * cs.y;
             float o1 = v1 * cs.x + v0 * cs.y;
             if (r0 < a.qd) {
@@ -251,7 +267,18 @@ __device__ inline void gv_epilogue(const GemvArgs &a, int rg, float v0, float v1
 // layout [g = 2b (hi), 2b+1 (lo)][t][16 bytes] plus, once, the block factor
 // 2^-e.  The per-warp sums of x^2 (for RMSNorm) go to red.
 // ---------------------------------------------------------------------------
-__device__ inline void gv_operand(const GemvArgs &a, const GvScratch &s, int tid, int nthreads) {
+// Default source of the operand: 8 consecutive elements k.. of column b of x.
+struct GvLoadX {
+    __device__ void operator()(const GemvArgs &a, int b, int k, float (&v)[8]) const {
+        const float4 *xp = reinterpret_cast<const float4 *>(a.x + (size_t)(a.b0 + b) * a.K + k);
+        const float4 x0 = __ldcg(xp), x1 = __ldcg(xp + 1);
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    }
+};
+
+template <class Load>
+__device__ inline void gv_operand(const GemvArgs &a, const GvScratch &s, int tid, int nthreads, const Load &load) {
     const int K = a.K, B = a.B, nbp = gv_nbp(K), nb = K / 32;
     const int lane = tid & 31, warp = tid >> 5;
     float *sx = reinterpret_cast<float *>(s.xs + (size_t)nbp * B * 128);
@@ -269,10 +296,13 @@ __device__ inline void gv_operand(const GemvArgs &a, const GvScratch &s, int tid
         for (int i = 0; i < 8; ++i) v[i] = 0.f;
         if (ok && kb < nb) {
             const int k = kb * 32 + q * 8;
-            const float4 *xp = reinterpret_cast<const float4 *>(a.x + (size_t)(a.b0 + b) * K + k);
-            const float4 x0 = __ldcg(xp), x1 = __ldcg(xp + 1);
-            v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-            v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+            float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+            if (a.gain) {  // constant data: requested ahead of x
+                const float4 *gp = reinterpret_cast<const float4 *>(a.gain + k);
+                g0 = __ldg(gp);
+                g1 = __ldg(gp + 1);
+            }
+            load(a, b, k, v);
             float sq = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) sq = fmaf(v[i], v[i], sq);
@@ -280,8 +310,6 @@ __device__ inline void gv_operand(const GemvArgs &a, const GvScratch &s, int tid
             for (int bb = 0; bb < GV_MAXB; ++bb)
                 if (bb == b) ssq[bb] += sq;
             if (a.gain) {
-                const float4 *gp = reinterpret_cast<const float4 *>(a.gain + k);
-                const float4 g0 = gp[0], g1 = gp[1];
                 v[0] *= g0.x; v[1] *= g0.y; v[2] *= g0.z; v[3] *= g0.w;
                 v[4] *= g1.x; v[5] *= g1.y; v[6] *= g1.z; v[7] *= g1.w;
             }
@@ -323,6 +351,10 @@ __device__ inline void gv_operand(const GemvArgs &a, const GvScratch &s, int tid
         for (int off = 16; off; off >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, off);
         if (lane == 0) s.red[(warp * GV_MAXB + b) * 2] = sm;
     }
+}
+
+__device__ inline void gv_operand(const GemvArgs &a, const GvScratch &s, int tid, int nthreads) {
+    gv_operand(a, s, tid, nthreads, GvLoadX{});
 }
 
 // RMSNorm factor 1 / sqrt(mean(x^2) + eps) of column b (1 without a gain)
@@ -397,11 +429,11 @@ __device__ inline void gv_unit(uint32_t ub, uint32_t xa, uint32_t kb_stride, uin
 // ---------------------------------------------------------------------------
 template <int QT, int EPI, class Refill>
 __device__ inline int gv_consume(const GemvArgs &a, const GvScratch &s, const GvRange &r, uint8_t *ring,
-                                 uint64_t *wbar, long long k0, Refill refill, int lane, int warp) {
+                                 uint64_t *wbar, unsigned k0, Refill refill, int lane, int warp) {
     using C = GvCfg<QT>;
     const int UPR = a.UPR;
     const int g = lane >> 2, t = lane & 3;
-    const int nunits = (int)(r.wb - r.wa);
+    const int nunits = r.wb - r.wa;
     const int nslots = (nunits + C::SU - 1) / C::SU;
     if (nslots == 0) return 0;
     const bool has_b = g < 2 * a.B;
@@ -411,10 +443,10 @@ __device__ inline int gv_consume(const GemvArgs &a, const GvScratch &s, const Gv
     const uint32_t sx_lane = smem_u32(s.xs) + (uint32_t)(gv_nbp(a.K) * a.B * 128 + tb * 8);
     const uint32_t sx_stride = (uint32_t)(a.B * 8);  // per unit
     const float f = gv_rstd(a, s, tb, GV_WARPS);
-    const long long rg_first = r.wa / UPR;
+    const int rg_first = r.rgf;
 
     auto leave = [&](int rgf, float v0, float v1) {
-        const long long r_lo = (long long)rgf * UPR, r_hi = r_lo + UPR;
+        const int r_lo = rgf * UPR, r_hi = r_lo + UPR;
         if (r_lo >= r.wa && r_hi <= r.wb) {
             gv_epilogue<EPI>(a, rgf, v0, v1, f, lane);
             return;
@@ -425,12 +457,12 @@ __device__ inline int gv_consume(const GemvArgs &a, const GvScratch &s, const Gv
     };
 
     float acc0 = 0.f, acc1 = 0.f, accb0 = 0.f, accb1 = 0.f;
-    int rg = (int)rg_first;
-    int j = (int)(r.wa - (long long)rg * UPR);
+    int rg = rg_first;
+    int j = r.j0;
     for (int k = 0; k < nslots; ++k) {
-        const long long kg = k0 + k;
-        const int sidx = (int)(kg % GV_SLOTS);
-        if (!mbar_wait(wbar + sidx, (uint32_t)((kg / GV_SLOTS) & 1))) {
+        const unsigned kg = k0 + (unsigned)k;
+        const unsigned sidx = kg % GV_SLOTS;
+        if (!mbar_wait(wbar + sidx, (kg / GV_SLOTS) & 1u)) {
             if (lane == 0) atomicOr(a.flags, ER_FLAG_WAIT);
             return -1;
         }
@@ -474,17 +506,17 @@ __device__ inline void gv_finish_shared(const GemvArgs &a, const GvScratch &s, c
                                         int max_ctas, int lane, int warp) {
     if (!r.working) return;
     const int UPR = a.UPR;
-    const long long U = (long long)a.R * UPR;
+    const int U = a.R * UPR;
     const int nC = gv_ctas(a.R, UPR, max_ctas);
-    const long long cfirst = r.ca / UPR;
+    const int cfirst = r.ca / UPR;
     const int t = lane & 3;
     const float f = gv_rstd(a, s, t < a.B ? t : a.B - 1, GV_WARPS);
     for (int slot = 0; slot < 2; ++slot) {
         const int rgf = s.wrg[warp * 2 + slot];
         if (rgf < 0) continue;
-        const long long r_lo = (long long)rgf * UPR, r_hi = r_lo + UPR;
-        const int lo_local = (int)((r_lo > r.ca ? r_lo : r.ca) - r.ca);
-        const int hi_local = (int)((r_hi < r.cb ? r_hi : r.cb) - r.ca);
+        const int r_lo = rgf * UPR, r_hi = r_lo + UPR;
+        const int lo_local = (r_lo > r.ca ? r_lo : r.ca) - r.ca;
+        const int hi_local = (r_hi < r.cb ? r_hi : r.cb) - r.ca;
         const int w_first = ((lo_local + 1) * r.nw - 1) / r.n;
         if (w_first != warp) continue;
         const int w_last = (hi_local * r.nw - 1) / r.n;
@@ -505,10 +537,10 @@ __device__ inline void gv_finish_shared(const GemvArgs &a, const GvScratch &s, c
         if (lane == 0) old = atom_add_acq_rel_gpu(a.cnt + rgf, 1);  // releases the partial
         old = __shfl_sync(0xffffffffu, old, 0);
         __syncwarp();
-        const long long c_first = ((r_lo + 1) * nC - 1) / U, c_last = (r_hi * nC - 1) / U;
+        const int c_first = ((r_lo + 1) * nC - 1) / U, c_last = (r_hi * nC - 1) / U;
         if (old == (int)(c_last - c_first)) {  // the acquire above orders these loads after every partial
             float s0 = 0.f, s1 = 0.f;
-            for (long long c = c_first; c <= c_last; ++c) {
+            for (int c = c_first; c <= c_last; ++c) {
                 const int sl = ((c * U / nC) / UPR == rgf) ? 0 : 1;
                 const float *q = a.part + ((size_t)c * 2 + sl) * 64 + lane * 2;
                 s0 += __ldcg(q);

@@ -67,6 +67,12 @@ struct GemvArgs {
     float *part;
     int *cnt;
     int *flags;
+    // optional shared-memory copies (persistent step): positions and RoPE rows
+    // [b][hd / 2] of the step, and the residual rows [row group - resid_rg0][16][GV_MAXB]
+    const int *pos_s;
+    const float2 *rope_s;
+    const float *resid_s;
+    int resid_rg0, resid_nrg;
 };
 
 // B <= 4 per launch; returns cudaErrorInvalidValue for shapes it cannot take
@@ -118,15 +124,16 @@ struct StepArgs {
     int32_t *argmax;
     float *part;    // GEMV cross-CTA partials
     int *cnt;       // GEMV cross-CTA counters
-    float *apart;   // attention partial states [warps][2][G][hd + 2]
-    int *acnt;      // attention counters [B * KV]
+    float *apart;   // attention states of heads split over CTAs [CTA][2][G][hd + 4]
+    int *acnt;      // attention counters [B * KV] (unused by the persistent step)
     unsigned long long *amax;
     int *done, *flags;
     unsigned *bar;  // grid barrier counter (zeroed before each launch)
 };
 // Whether the persistent step can run this shape (batch, GQA group, head dim,
 // shared memory) and the launch itself (cooperative, one CTA per SM).
-bool step_supported(int qt, int hd, int G, int B, int max_k, int num_sms);
+bool step_supported(int qt, int hd, int G, int B, int KV, int cap, int max_k, const int R[5], const int UPR[5],
+                    int num_sms);
 cudaError_t launch_step(int qt, const StepArgs &a, int num_sms, cudaStream_t st);
 size_t step_apart_floats(int num_sms, int hd);
 cudaError_t step_prepare();

@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) gemv_kernel(const GemvArgs a
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const GvRange r = gv_range(a.R, a.UPR, blockIdx.x, max_ctas, warp);
-    const int nunits = (int)(r.wb - r.wa);
+    const int nunits = r.wb - r.wa;
     const int nslots = (nunits + C::SU - 1) / C::SU;
     uint64_t *wbar = bars + warp * GV_SLOTS;
     uint8_t *ring = smem + GV_OFF_RING + warp * GV_SLOTS * C::SLOT;
@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) gemv_kernel(const GemvArgs a
     }
     pdl_launch_dependents();
 
-    auto refill = [&](long long k) {
-        if (k + GV_SLOTS < nslots) {
+    auto refill = [&](unsigned k) {
+        if ((int)k + GV_SLOTS < nslots) {
             if (lane == 0) {
                 fence_proxy_async_smem();
                 issue((int)k + GV_SLOTS);
@@ -143,7 +143,7 @@ static cudaError_t gv_launch(const GemvArgs &a, int num_sms, cudaStream_t st, bo
 }
 
 cudaError_t launch_gemv(int epi, const GemvArgs &a, int num_sms, cudaStream_t st, bool pdl) {
-    if (!gemv_fits(a.qt, a.K, a.B)) return cudaErrorInvalidValue;
+    if (!gemv_fits(a.qt, a.K, a.B) || !gv_index_ok(a.R, a.UPR, num_sms)) return cudaErrorInvalidValue;
     if (a.qt == Q8_0) {
         switch (epi) {
             case EPI_STORE: return gv_launch<Q8_0, EPI_STORE>(a, num_sms, st, pdl);

@@ -87,21 +87,26 @@ cudaError_t step_prepare() {
 static size_t step_smem(int qt, int max_k, int B, int hd, int G) {
     return qt == Q8_0 ? mk_smem_bytes<Q8_0>(max_k, B, hd, G) : mk_smem_bytes<Q4_0>(max_k, B, hd, G);
 }
-// static shared memory of the step kernel (barrier flag, warp range table)
-constexpr size_t STEP_STATIC_SMEM = 8192;
+// static shared memory of the step kernel (barrier flag, warp ranges, per-step tables)
+constexpr size_t STEP_STATIC_SMEM = 12288;
 
-bool step_supported(int qt, int hd, int G, int B, int max_k, int num_sms) {
+bool step_supported(int qt, int hd, int G, int B, int KV, int cap, int max_k, const int R[5], const int UPR[5],
+                    int num_sms) {
     if (B < 1 || B > ER_MK_MAXB || G < 1 || G > ER_MK_MAXG || (hd != 64 && hd != 128)) return false;
+    // 32-bit row and unit indices, byte-sized CTA indices in the segment table
+    if (num_sms > 255 || B * KV > MK_MAX_SEGS) return false;
+    if ((long long)B * KV * cap * (num_sms + 1) >= (1ll << 31)) return false;
+    for (int i = 0; i < 5; ++i)
+        if (!gv_index_ok(R[i], UPR[i], num_sms)) return false;
     if (step_smem(qt, max_k, B, hd, G) + STEP_STATIC_SMEM > 227 * 1024) return false;
     // cooperative launch: one CTA of the kernel must fit on every SM (each
     // weight type's kernels are instantiated, and configured, in their own file)
     const size_t smem = step_smem(qt, max_k, B, hd, G);
     const int per_sm = qt == Q8_0 ? step_occupancy_q8(hd, smem) : step_occupancy_q4(hd, smem);
-    (void)num_sms;
     return per_sm >= 1;
 }
 
-size_t step_apart_floats(int num_sms, int hd) { return (size_t)num_sms * GV_WARPS * 2 * ER_MK_MAXG * (hd + 2); }
+size_t step_apart_floats(int num_sms, int hd) { return (size_t)num_sms * 2 * ER_MK_MAXG * (hd + 4); }
 
 cudaError_t launch_step(int qt, const StepArgs &a, int num_sms, cudaStream_t st) {
     const int max_k = a.D > a.qd ? (a.D > a.F ? a.D : a.F) : (a.qd > a.F ? a.qd : a.F);

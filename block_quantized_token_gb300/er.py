@@ -65,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "er_positions_increment": (I32, [VP, I32, VP]),
         "er_kv_set_schedule": (I32, [VP, I32]),
         "er_kv_get_schedule": (I32, [VP]),
+        "er_kv_launches_per_step": (I32, [VP]),
         "er_get_device_error": (I32, [VP, P(I32), P(I32)]),
         "er_launch_stage": (I32, [VP, I32, I32, VP, VP, VP, VP, VP]),
         "er_matrix_create": (I32, [I32, I32, I32, VP, VP, P(VP)]),
@@ -87,7 +88,7 @@ EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_
             "er_kv_layer_ptrs", "er_kv_write", "er_kv_read", "er_decode_step", "er_decode_step_eager", "er_positions_increment",
             "er_kv_set_schedule", "er_kv_get_schedule",
             "er_get_device_error", "er_launch_stage", "er_matrix_create", "er_matrix_destroy",
-            "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_status_str", "er_last_error")
+            "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_kv_launches_per_step", "er_status_str", "er_last_error")
 
 
 def lib() -> ctypes.CDLL:
@@ -168,6 +169,10 @@ def er_kv_set_schedule(kv: int, schedule: int) -> None:
 
 def er_kv_get_schedule(kv: int) -> int:
     return _lib.er_kv_get_schedule(kv)
+
+
+def er_kv_launches_per_step(kv: int) -> int:
+    return int(_lib.er_kv_launches_per_step(kv))
 
 
 def er_get_device_error(kv: int) -> tuple[int, int, int]:

@@ -163,6 +163,12 @@ typedef enum { ER_SCHEDULE_AUTO = 0, ER_SCHEDULE_PERSISTENT = 1, ER_SCHEDULE_KER
 ER_API er_status er_kv_set_schedule(er_kv *kv, int32_t schedule);
 /* The schedule in effect (ER_SCHEDULE_PERSISTENT or ER_SCHEDULE_KERNELS), or -1 for NULL. */
 ER_API int32_t er_kv_get_schedule(const er_kv *kv);
+/* Kernel launches one er_decode_step enqueues under the schedule in effect
+ * (memsets not counted), or -1 for NULL: 1 for the persistent schedule; for
+ * the per-phase one, the embedding, per layer the QKV, attention, Wo, gate/up
+ * and down launches (a GEMV takes one launch per group of at most 4 batch
+ * columns that fit its shared memory), and the head. */
+ER_API int32_t er_kv_launches_per_step(const er_kv *kv);
 
 /* positions_dev[b] += 1 for b < batch (chains steps without a host round trip). */
 ER_API er_status er_positions_increment(int32_t *positions_dev, int32_t batch, void *stream);
