@@ -42,6 +42,7 @@ from .gen import (  # noqa: F401
     ModelShape,
     Workload,
     kv_prefill,
+    model_weights,
     quantize,
     quantize_q4_0,
     quantize_q8_0,
