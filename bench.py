@@ -152,11 +152,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     wl_run = wl.with_(steps=cap - wl.prefill)
 
     t0 = time.time()
-    model = runtime.DecodeModel(s, lambda n: synth.weight_tensor(s, n), max_batch=B)
+    threads = min(32, os.cpu_count() or 1)
+    model = runtime.DecodeModel(s, synth.model_weights(s, threads=threads), max_batch=B)
     state = runtime.DecodeState(model, B, cap)
-    for b in range(B):
-        for l in range(s.n_layers):
-            k, v = synth.kv_prefill(wl_run, b, l)
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=threads) as ex:  # draws run in parallel, writes in order
+        jobs = [(b, l) for b in range(B) for l in range(s.n_layers)]
+        for (b, l), (k, v) in zip(jobs, ex.map(lambda bl: synth.kv_prefill(wl_run, *bl), jobs)):
             state.write_rows(b, l, k, v)
     setup_s = time.time() - t0
 

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <string>
 
 #include "common.cuh"
@@ -265,6 +266,28 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
     A(&kv->attn_cnt, (size_t)batch * c.n_kv_heads * sizeof(int));
     A(&kv->gemv_part, gemv_part_floats(m->num_sms) * sizeof(float));
     A(&kv->gemv_cnt, (size_t)max_r * sizeof(int));
+    // batched GEMV (one pass over the weights for the whole batch) where every matrix takes it
+    kv->wide_part = kv->wide_ssq = nullptr;
+    if (batch > 4) {  // more columns than one pass of the batch-1 GEMV takes
+        bool ok = true;
+        size_t part = 0, ssq = 0;
+        auto need = [&](const er::Mat &w) {
+            ok = ok && gemv_wide_fits(w.qt, w.K, batch, m->num_sms);
+            part = std::max(part, gemv_wide_part_floats(w.R, w.K));
+            ssq = std::max(ssq, gemv_wide_ssq_floats(w.K));
+        };
+        for (int l = 0; l < c.n_layers; ++l) {
+            need(m->layers[l].qkv);
+            need(m->layers[l].wo);
+            need(m->layers[l].gateup);
+            need(m->layers[l].down);
+        }
+        need(m->head);
+        if (ok) {
+            A(&kv->wide_part, std::max<size_t>(part, 1) * sizeof(float), false);
+            A(&kv->wide_ssq, ssq * sizeof(float), false);
+        }
+    }
     A(&kv->amax, 16 * sizeof(unsigned long long));
     A(&kv->done, sizeof(int));
     A(&kv->flags, sizeof(int));
@@ -395,8 +418,14 @@ static GemvArgs gemv_base(er_kv *kv, const Mat &w) {
     return a;
 }
 
-// one GEMV over the whole batch, in as few column groups as the kernel takes
+// one GEMV over the whole batch: one pass for a batch of more than 4 columns
+// where the batched kernel takes it, else as few column groups as the kernel takes
 static cudaError_t gemv_all(er_kv *kv, int epi, GemvArgs a, cudaStream_t st, bool pdl) {
+    if (kv->wide_part) {
+        a.b0 = 0;
+        a.B = kv->B;
+        return launch_gemv_wide(epi, a, kv->wide_part, kv->wide_ssq, kv->m->num_sms, st, pdl);
+    }
     int per = gemv_max_cols(a.qt, a.K);
     for (int b0 = 0; b0 < kv->B; b0 += per) {
         a.b0 = b0;
@@ -642,6 +671,7 @@ int32_t er_kv_launches_per_step(const er_kv *kv) {
     const er_model *m = kv->m;
     const er_config &c = m->cfg;
     auto groups = [&](const er::Mat &w) {
+        if (kv->wide_part) return 1;
         const int per = gemv_max_cols(w.qt, w.K);
         return per > 0 ? (kv->B + per - 1) / per : 0;
     };

@@ -77,6 +77,15 @@ struct GemvArgs {
 
 // B <= 4 per launch; returns cudaErrorInvalidValue for shapes it cannot take
 cudaError_t launch_gemv(int epi, const GemvArgs &a, int num_sms, cudaStream_t st, bool pdl);
+// The whole batch (up to 16 columns, b0 = 0) in one pass over the weights:
+// K-slices of 1024 columns, partials wpart (gemv_wide_part_floats), per-slice
+// sums of squares wssq (gemv_wide_ssq_floats), counters a.cnt [R] (zero).
+cudaError_t launch_gemv_wide(int epi, const GemvArgs &a, float *wpart, float *wssq, int num_sms, cudaStream_t st,
+                             bool pdl);
+cudaError_t gemv_wide_prepare();
+bool gemv_wide_fits(int qt, int K, int B, int num_sms);
+size_t gemv_wide_part_floats(int R, int K);
+size_t gemv_wide_ssq_floats(int K);
 cudaError_t gemv_prepare();  // sets kernel attributes once (call before any capture)
 size_t gemv_part_floats(int num_sms);
 bool gemv_fits(int qt, int K, int B);
@@ -208,6 +217,7 @@ struct er_kv {
     int *attn_cnt;
     float *gemv_part;
     int *gemv_cnt;
+    float *wide_part, *wide_ssq;  // batched GEMV scratch (nullptr: column groups instead)
     unsigned long long *amax;
     int *done;
     int *flags;

@@ -110,6 +110,7 @@ cudaError_t gemv_prepare() {
                          gv_attr<Q4_0, EPI_LOGITS>()};
     for (cudaError_t x : r)
         if (x != cudaSuccess) e = x;
+    if (e == cudaSuccess) e = gemv_wide_prepare();
     if (e == cudaSuccess) e = attention_prepare();
     if (e == cudaSuccess) e = step_prepare();
     return e;

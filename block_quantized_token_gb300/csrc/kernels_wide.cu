@@ -1,0 +1,419 @@
+// Batched decode GEMV for 5..16 sequences: y[b] = W x[b] for every column b of
+// the batch in one pass over the weights ("EdgeRunner Core Architecture"
+// section 5.1 projections, decode of several sequences at once).
+//
+// With 16 columns the activation operand of a whole row (K up to 14336)
+// does not fit in shared memory, so the matrix is cut into K-slices of 1024
+// columns (16 units).  Slice s is worked by a contiguous group of CTAs, each
+// taking a contiguous range of row groups; its warps take whole row groups in
+// turn and stream the slice's units of each through their ring of bulk-copy
+// slots (as the batch-1 GEMV does).  The unit's weights are turned into exact
+// fp16 once and multiplied against NT n8 tiles of operand columns (hi and lo
+// fp16 halves of each batch column).  A row group's slice partial (16 rows x
+// 16 columns, already scaled) goes to global memory; the last slice to arrive
+// at the row group's counter sums the partials in slice order and runs the
+// epilogue, so the result does not depend on timing.
+//
+// Operand: per CTA, once, for its slice: every column's elements of the slice
+// times the RMSNorm gain, scaled by one power of two per column (largest
+// element in [2^14, 2^15)) and split into hi + lo fp16.  The slice's sum of
+// squares of x per column goes to global memory for the finisher's 1/rms.
+#include "gemv_core.cuh"
+
+namespace er {
+
+constexpr int GW_WARPS = 16;
+constexpr int GW_SLICE_UNITS = 16;            // 1024 columns
+constexpr int GW_NT = 4;                      // n8 tiles: 16 batch columns x (hi, lo)
+constexpr int GW_BLOCK_BYTES = GW_NT * 8 * 64;  // operand bytes of one 32-element block
+constexpr int GW_OFF_RING = 512;
+
+__host__ __device__ inline int gw_slices(int UPR) { return (UPR + GW_SLICE_UNITS - 1) / GW_SLICE_UNITS; }
+
+template <int QT>
+constexpr int gw_off_operand() { return GW_OFF_RING + GvCfg<QT>::RING; }
+template <int QT>
+constexpr int gw_smem() {
+    // operand of 32 blocks, then per-column factors [16], column maxima [16] (uint), per-item sums of squares [512]
+    return gw_off_operand<QT>() + 2 * GW_SLICE_UNITS * GW_BLOCK_BYTES + 16 * 4 + 16 * 4 + 512 * 4 + 64;
+}
+
+// first CTA of slice s when C CTAs share S slices
+__host__ __device__ inline int gw_cta0(int s, int S, int C) { return (int)((long long)s * C / S); }
+
+// One unit (16 rows x 2 blocks): acc[j][0/1] += d(row) * (hi + lo sums) for tile j.
+template <int QT>
+__device__ inline void gw_unit(uint32_t ub, uint32_t xop, int lane, float (&acc)[GW_NT][2]) {
+    const int g = lane >> 2;
+    const uint2 sc = lds64(ub + GvCfg<QT>::QB + g * 8);
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint4 q0, q1;
+    if (QT == Q8_0) {
+        q0 = lds128(ub + lane * 16);
+        q1 = lds128(ub + 512 + lane * 16);
+    } else {
+        q0 = lds128(ub + lane * 16);
+    }
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        uint32_t a0[4], a1[4];
+        if (QT == Q8_0) {
+            const uint4 q = blk ? q1 : q0;
+            q8_word_to_h2(q.x, a0[0], a0[1]);
+            q8_word_to_h2(q.y, a0[2], a0[3]);
+            q8_word_to_h2(q.z, a1[0], a1[1]);
+            q8_word_to_h2(q.w, a1[2], a1[3]);
+        } else {
+            q4_word_to_h2(blk ? q0.z : q0.x, a0);
+            q4_word_to_h2(blk ? q0.w : q0.y, a1);
+        }
+        const uint32_t sch = blk ? sc.y : sc.x;
+        const float dg = h2f_lo(sch), dg8 = h2f_hi(sch);
+        uint4 xb[GW_NT];
+#pragma unroll
+        for (int j = 0; j < GW_NT; ++j) xb[j] = lds128(xop + blk * GW_BLOCK_BYTES + j * 8 * 64);
+#pragma unroll
+        for (int j = 0; j < GW_NT; ++j) {
+            float c[4];
+            mma_16816(c, a0, xb[j].x, xb[j].y, zero4);
+            mma_16816(c, a1, xb[j].z, xb[j].w, c);
+            acc[j][0] = fmaf(dg, c[0] + c[1], acc[j][0]);
+            acc[j][1] = fmaf(dg8, c[2] + c[3], acc[j][1]);
+        }
+    }
+}
+
+// Argmax part of the head epilogue for the whole batch of one row group, then
+// one count per row group; the last row group writes the argmax of every column.
+__device__ inline void gw_logits(const GemvArgs &a, int rg, const float (&v)[GW_NT][2], const float (&f)[GW_NT],
+                                 int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < GW_NT; ++j) {
+        const int b = 4 * j + t;
+        unsigned long long key = 0;
+        if (b < a.B) {
+            const int r0 = 16 * rg + g, r1 = r0 + 8;
+            const float v0 = v[j][0] * f[j], v1 = v[j][1] * f[j];
+            float *y = a.y ? a.y + (size_t)b * a.N : nullptr;
+            bool bad = false;
+            if (r0 < a.N) {
+                if (y) y[r0] = v0;
+                bad |= !isfinite(v0);
+                key = ((unsigned long long)float_order_key(isnan(v0) ? -INFINITY : v0) << 32) |
+                      (0xFFFFFFFFu - (uint32_t)r0);
+            }
+            if (r1 < a.N) {
+                if (y) y[r1] = v1;
+                bad |= !isfinite(v1);
+                const unsigned long long k1 = ((unsigned long long)float_order_key(isnan(v1) ? -INFINITY : v1) << 32) |
+                                              (0xFFFFFFFFu - (uint32_t)r1);
+                key = k1 > key ? k1 : key;
+            }
+            if (bad) atomicOr(a.flags, ER_FLAG_NONFINITE);
+        }
+        for (int off = 4; off < 32; off <<= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+            key = o > key ? o : key;
+        }
+        if (b < a.B && g == 0 && key) atomicMax(a.amax + b, key);
+    }
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atom_add_acq_rel_gpu(a.done, 1) == a.R - 1;  // releases this warp's maxima
+    last = __shfl_sync(0xffffffffu, last, 0);
+    __syncwarp();
+    if (last) {
+        if (lane < a.B) {
+            const unsigned long long k = atomicExch(a.amax + lane, 0ull);
+            const int idx = k ? (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu)) : 0;
+            if (a.argmax_out) a.argmax_out[lane] = idx;
+        }
+        if (lane == 0) *a.done = 0;
+    }
+}
+
+template <int QT, int EPI>
+__global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvArgs a, float *wpart, float *wssq) {
+    using C = GvCfg<QT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *op = smem + gw_off_operand<QT>();
+    float *fac = reinterpret_cast<float *>(op + 2 * GW_SLICE_UNITS * GW_BLOCK_BYTES);
+    unsigned *cmax = reinterpret_cast<unsigned *>(fac + 16);
+    float *issq = reinterpret_cast<float *>(cmax + 16);
+    __shared__ int stop_s;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = gw_slices(a.UPR), nC = gridDim.x;
+    int s = 0;
+    while (s + 1 < S && gw_cta0(s + 1, S, nC) <= (int)blockIdx.x) ++s;
+    const int c0 = gw_cta0(s, S, nC), ns = gw_cta0(s + 1, S, nC) - c0, j = blockIdx.x - c0;
+    const int rg0 = (int)((long long)j * a.R / ns), rg1 = (int)((long long)(j + 1) * a.R / ns);
+    const int ku0 = s * GW_SLICE_UNITS, nu = min(GW_SLICE_UNITS, a.UPR - ku0);
+    const int nrg = rg1 - rg0;
+    const int my_items = nrg > warp ? (nrg - warp + GW_WARPS - 1) / GW_WARPS : 0;  // rows groups rg0 + warp + 16 i
+    const int spi = (nu + C::SU - 1) / C::SU;                                          // ring slots per row group
+
+    uint64_t *wbar = bars + warp * GV_SLOTS;
+    uint8_t *ring = smem + GW_OFF_RING + warp * GV_SLOTS * C::SLOT;
+    int p_item = 0, p_slot = 0, issued = 0;
+    auto issue_next = [&]() {  // lane 0
+        if (p_item >= my_items) return;
+        const int rg = rg0 + warp + GW_WARPS * p_item;
+        const int u0 = p_slot * C::SU, cnt = min(C::SU, nu - u0);
+        const uint32_t bytes = (uint32_t)cnt * C::UB;
+        const unsigned sidx = (unsigned)issued % GV_SLOTS;
+        mbar_arrive_expect_tx(wbar + sidx, bytes);
+        bulk_g2s(ring + sidx * C::SLOT, a.W + ((size_t)rg * a.UPR + ku0 + u0) * C::UB, bytes, wbar + sidx);
+        ++issued;
+        if (++p_slot == spi) {
+            p_slot = 0;
+            ++p_item;
+        }
+    };
+    if (lane == 0) {
+        for (int i = 0; i < GV_SLOTS; ++i) mbar_init(wbar + i, 1);
+        fence_mbar_init();
+        for (int i = 0; i < GV_SLOTS; ++i) issue_next();
+    }
+    __syncwarp();
+
+    // ---- everything above touches only constant weights; now wait for inputs
+    pdl_wait();
+    if (tid == 0) stop_s = *reinterpret_cast<volatile int *>(a.flags) & ER_FLAG_WAIT;
+    if (tid < 16) cmax[tid] = 0u;
+    // zero the operand columns past the batch (their MMA results are never read, but must be finite)
+    const int nbs = (nu * 64) / 32;  // blocks in this slice
+    if (2 * a.B < GW_NT * 8)
+        for (int i = tid; i < nbs * (GW_NT * 8 - 2 * a.B) * 16; i += blockDim.x) {
+            const int per = (GW_NT * 8 - 2 * a.B) * 16, kb = i / per, r = i - kb * per;
+            reinterpret_cast<uint32_t *>(op + kb * GW_BLOCK_BYTES + 2 * a.B * 64)[r] = 0u;
+        }
+    __syncthreads();
+    // one thread per (block, column): 32 elements of x, their gain, sum of squares and largest |x g|
+    const int kb = tid / a.B, b = tid - kb * a.B;
+    const bool item = kb < nbs;
+    float v[32];
+    float ssq = 0.f, m = 0.f;
+    if (item) {
+        const int k = ku0 * 64 + kb * 32;
+        const float4 *xp = reinterpret_cast<const float4 *>(a.x + (size_t)b * a.K + k);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 x4 = __ldcg(xp + i);
+            v[4 * i] = x4.x; v[4 * i + 1] = x4.y; v[4 * i + 2] = x4.z; v[4 * i + 3] = x4.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ssq = fmaf(v[i], v[i], ssq);
+        if (a.gain) {
+            const float4 *gp = reinterpret_cast<const float4 *>(a.gain + k);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g4 = __ldg(gp + i);
+                v[4 * i] *= g4.x; v[4 * i + 1] *= g4.y; v[4 * i + 2] *= g4.z; v[4 * i + 3] *= g4.w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+        if (!isfinite(m)) m = 0.f;
+        atomicMax(cmax + b, __float_as_uint(m));  // non-negative floats order as their bits
+    }
+    issq[tid] = ssq;
+    __syncthreads();
+    if (tid < a.B) {
+        float t = 0.f;
+        for (int i = tid; i < nbs * a.B; i += a.B) t += issq[i];  // block order: deterministic
+        wssq[s * 16 + tid] = t;  // every CTA of the slice writes the same value
+        const float mx = __uint_as_float(cmax[tid]);
+        int e = 0;
+        if (mx > 0.f) {
+            int E;
+            frexpf(mx, &E);
+            e = 15 - E;
+        }
+        fac[tid] = ldexpf(1.f, -e);
+    }
+    __syncthreads();
+    if (item) {
+        const float sc = 1.f / fac[b];
+        uint8_t *area = op + kb * GW_BLOCK_BYTES + 2 * b * 64;
+#pragma unroll
+        for (int p = 0; p < 16; ++p) {  // element pair (2p, 2p+1) of the block
+            const int h = p >> 3, w8 = p & 7, reg = w8 >> 2, tt = w8 & 3;
+            const float v0 = v[2 * p] * sc, v1 = v[2 * p + 1] * sc;
+            const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+            const __half l0 = __float2half_rn(v0 - __half2float(h0));
+            const __half l1 = __float2half_rn(v1 - __half2float(h1));
+            const int off = tt * 16 + (h * 2 + reg) * 4;
+            *reinterpret_cast<__half2 *>(area + off) = __halves2half2(h0, h1);
+            *reinterpret_cast<__half2 *>(area + 64 + off) = __halves2half2(l0, l1);
+        }
+    }
+    __syncthreads();
+    if (stop_s) {  // an earlier kernel gave up on a wait: drain and stop
+        if (lane == 0)
+            for (int k = 0; k < issued; ++k) mbar_wait(wbar + k % GV_SLOTS, (k / GV_SLOTS) & 1);
+        return;
+    }
+    pdl_launch_dependents();
+
+    // ---- consume: whole row groups, slice units in order
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t xop = smem_u32(op) + (uint32_t)(g * 64 + t * 16);
+    float fj[GW_NT];
+#pragma unroll
+    for (int jj = 0; jj < GW_NT; ++jj) fj[jj] = (4 * jj + t < a.B) ? fac[4 * jj + t] : 0.f;
+    int k = 0;  // ring slot counter
+    bool failed = false;
+    for (int it = 0; it < my_items && !failed; ++it) {
+        const int rg = rg0 + warp + GW_WARPS * it;
+        float acc[GW_NT][2];
+#pragma unroll
+        for (int jj = 0; jj < GW_NT; ++jj) acc[jj][0] = acc[jj][1] = 0.f;
+        for (int sl = 0; sl < spi; ++sl, ++k) {
+            const unsigned sidx = (unsigned)k % GV_SLOTS;
+            if (!mbar_wait(wbar + sidx, ((unsigned)k / GV_SLOTS) & 1u)) {
+                if (lane == 0) atomicOr(a.flags, ER_FLAG_WAIT);
+                failed = true;
+                break;
+            }
+            const int u0 = sl * C::SU, cnt = min(C::SU, nu - u0);
+            const uint32_t sb = smem_u32(ring + sidx * C::SLOT);
+            for (int i = 0; i < cnt; ++i)
+                gw_unit<QT>(sb + i * C::UB, xop + (uint32_t)(2 * (u0 + i)) * GW_BLOCK_BYTES, lane, acc);
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue_next();
+            }
+        }
+        if (failed) break;
+        float v2[GW_NT][2];
+        if (S == 1) {
+#pragma unroll
+            for (int jj = 0; jj < GW_NT; ++jj) {
+                v2[jj][0] = acc[jj][0] * fj[jj];
+                v2[jj][1] = acc[jj][1] * fj[jj];
+            }
+        } else {
+            // this slice's partial [lane][tile][2]; the last slice to arrive sums them in slice order
+            float4 *pp = reinterpret_cast<float4 *>(wpart + ((size_t)s * a.R + rg) * 256 + lane * 8);
+            pp[0] = make_float4(acc[0][0] * fj[0], acc[0][1] * fj[0], acc[1][0] * fj[1], acc[1][1] * fj[1]);
+            pp[1] = make_float4(acc[2][0] * fj[2], acc[2][1] * fj[2], acc[3][0] * fj[3], acc[3][1] * fj[3]);
+            __syncwarp();
+            int old = 0;
+            if (lane == 0) old = atom_add_acq_rel_gpu(a.cnt + rg, 1);  // releases the partial
+            old = __shfl_sync(0xffffffffu, old, 0);
+            __syncwarp();
+            if (old != S - 1) continue;
+#pragma unroll
+            for (int jj = 0; jj < GW_NT; ++jj) v2[jj][0] = v2[jj][1] = 0.f;
+            for (int ss = 0; ss < S; ++ss) {
+                const float4 *qp = reinterpret_cast<const float4 *>(wpart + ((size_t)ss * a.R + rg) * 256 + lane * 8);
+                const float4 p0 = __ldcg(qp), p1 = __ldcg(qp + 1);
+                v2[0][0] += p0.x; v2[0][1] += p0.y; v2[1][0] += p0.z; v2[1][1] += p0.w;
+                v2[2][0] += p1.x; v2[2][1] += p1.y; v2[3][0] += p1.z; v2[3][1] += p1.w;
+            }
+            if (lane == 0) a.cnt[rg] = 0;
+        }
+        // 1/rms of each of this lane's columns, from the slices' sums of squares (slice order)
+        float f[GW_NT];
+#pragma unroll
+        for (int jj = 0; jj < GW_NT; ++jj) {
+            f[jj] = 1.f;
+            const int bb = 4 * jj + t;
+            if (a.gain && bb < a.B) {
+                float t2 = 0.f;
+                for (int ss = 0; ss < S; ++ss) t2 += __ldcg(wssq + ss * 16 + bb);
+                f[jj] = 1.f / sqrtf(t2 / (float)a.K + a.eps);
+            }
+        }
+        if (EPI == EPI_LOGITS) {
+            gw_logits(a, rg, v2, f, lane);
+        } else {
+#pragma unroll
+            for (int jj = 0; jj < GW_NT; ++jj) {
+                if (4 * jj >= a.B) break;
+                GemvArgs a4 = a;
+                a4.b0 = 4 * jj;
+                a4.B = min(4, a.B - 4 * jj);
+                gv_epilogue<EPI>(a4, rg, v2[jj][0], v2[jj][1], f[jj], lane);
+            }
+        }
+    }
+    if (failed && lane == 0)
+        for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % GV_SLOTS, (kk / GV_SLOTS) & 1);
+}
+
+// ---------------------------------------------------------------------------
+template <int QT, int EPI>
+static cudaError_t gw_attr() {
+    cudaError_t e = cudaFuncSetAttribute(gemv_wide_kernel<QT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         gw_smem<QT>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemv_wide_kernel<QT, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    return e;
+}
+
+cudaError_t gemv_wide_prepare() {
+    cudaError_t r[10] = {gw_attr<Q8_0, EPI_STORE>(), gw_attr<Q8_0, EPI_RESID>(), gw_attr<Q8_0, EPI_QKV>(),
+                         gw_attr<Q8_0, EPI_SWIGLU>(), gw_attr<Q8_0, EPI_LOGITS>(), gw_attr<Q4_0, EPI_STORE>(),
+                         gw_attr<Q4_0, EPI_RESID>(), gw_attr<Q4_0, EPI_QKV>(), gw_attr<Q4_0, EPI_SWIGLU>(),
+                         gw_attr<Q4_0, EPI_LOGITS>()};
+    for (cudaError_t x : r)
+        if (x != cudaSuccess) return x;
+    return cudaSuccess;
+}
+
+bool gemv_wide_fits(int qt, int K, int B, int num_sms) {
+    (void)qt;
+    const int S = gw_slices(K / 64);
+    // one thread per (block, column) of a slice; at least one CTA per slice
+    return B >= 1 && B <= 16 && K % 64 == 0 && 32 * B <= GW_WARPS * 32 && S <= num_sms &&
+           (K / 64 >= GW_SLICE_UNITS ? 2 * GW_SLICE_UNITS * B : 2 * (K / 64) * B) <= GW_WARPS * 32;
+}
+
+size_t gemv_wide_part_floats(int R, int K) { return gw_slices(K / 64) > 1 ? (size_t)gw_slices(K / 64) * R * 256 : 0; }
+size_t gemv_wide_ssq_floats(int K) { return (size_t)gw_slices(K / 64) * 16; }
+
+template <int QT, int EPI>
+static cudaError_t gw_launch(const GemvArgs &a, float *wpart, float *wssq, int num_sms, cudaStream_t st, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)num_sms);
+    cfg.blockDim = dim3(GW_WARPS * 32);
+    cfg.dynamicSmemBytes = gw_smem<QT>();
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_wide_kernel<QT, EPI>, a, wpart, wssq);
+}
+
+cudaError_t launch_gemv_wide(int epi, const GemvArgs &a, float *wpart, float *wssq, int num_sms, cudaStream_t st,
+                             bool pdl) {
+    if (!gemv_wide_fits(a.qt, a.K, a.B, num_sms) || a.b0 != 0) return cudaErrorInvalidValue;
+    if (a.qt == Q8_0) {
+        switch (epi) {
+            case EPI_STORE: return gw_launch<Q8_0, EPI_STORE>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_RESID: return gw_launch<Q8_0, EPI_RESID>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_QKV: return gw_launch<Q8_0, EPI_QKV>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_SWIGLU: return gw_launch<Q8_0, EPI_SWIGLU>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_LOGITS: return gw_launch<Q8_0, EPI_LOGITS>(a, wpart, wssq, num_sms, st, pdl);
+        }
+    } else {
+        switch (epi) {
+            case EPI_STORE: return gw_launch<Q4_0, EPI_STORE>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_RESID: return gw_launch<Q4_0, EPI_RESID>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_QKV: return gw_launch<Q4_0, EPI_QKV>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_SWIGLU: return gw_launch<Q4_0, EPI_SWIGLU>(a, wpart, wssq, num_sms, st, pdl);
+            case EPI_LOGITS: return gw_launch<Q4_0, EPI_LOGITS>(a, wpart, wssq, num_sms, st, pdl);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace er

@@ -174,9 +174,12 @@ SMALL_SHAPES = {
 
 @pytest.mark.parametrize("schedule", [PERSISTENT, KERNELS], ids=["persistent", "kernels"])
 @pytest.mark.parametrize("name", list(SMALL_SHAPES))
-@pytest.mark.parametrize("batch", [1, 3, 6])
+@pytest.mark.parametrize("batch", [1, 3, 6, 16])
 def test_small_models_ragged_batch(name, batch, schedule):
-    """Tied/untied, Q4_0/Q8_0, G = 1/3/4, hd 64/128, odd sizes; sequences at different positions."""
+    """Tied/untied, Q4_0/Q8_0, G = 1/3/4, hd 64/128, odd sizes; sequences at different positions.
+
+    Batches above 4 run the one-pass batched GEMV where K is a multiple of 64
+    (the odd shape keeps the column-group path)."""
     shape = SMALL_SHAPES[name]
     wl = synth.Workload("t", shape, batch=batch, steps=3, prefill=37)
     if schedule == PERSISTENT and batch > 4:
@@ -193,7 +196,7 @@ def test_small_models_ragged_batch(name, batch, schedule):
     try:
         rng = np.random.default_rng(batch)
         tokens = rng.integers(0, shape.vocab, batch)
-        positions = np.array([37, 0, 5, 36, 12, 37][:batch])
+        positions = np.array([37, 0, 5, 36, 12, 37, 1, 20, 30, 7, 2, 33, 15, 9, 25, 37][:batch])
         dev = s.model.device
         t = torch.tensor(tokens, dtype=torch.int32, device=dev)
         p = torch.tensor(positions, dtype=torch.int32, device=dev)
