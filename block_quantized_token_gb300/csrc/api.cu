@@ -262,7 +262,7 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
     A(&kv->q, (size_t)batch * qd * sizeof(float));
     A(&kv->o, (size_t)batch * qd * sizeof(float));
     A(&kv->a, (size_t)batch * F * sizeof(float));
-    A(&kv->attn_part, (size_t)batch * c.n_kv_heads * kv->S * G * (hd + 2) * sizeof(float));
+    A(&kv->attn_part, attention_part_floats(hd, G, m->num_sms) * sizeof(float));
     A(&kv->attn_cnt, (size_t)batch * c.n_kv_heads * sizeof(int));
     A(&kv->gemv_part, gemv_part_floats(m->num_sms) * sizeof(float));
     A(&kv->gemv_cnt, (size_t)max_r * sizeof(int));

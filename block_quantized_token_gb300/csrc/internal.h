@@ -106,6 +106,7 @@ struct AttnArgs {
 };
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl);
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH);
+size_t attention_part_floats(int hd, int G, int num_sms);  // AttnArgs::part
 cudaError_t attention_prepare();  // kernel attributes (called by gemv_prepare)
 
 // ---------------------------------------------------------------------------

@@ -1,274 +1,362 @@
-// Split-K GQA decode attention over the fp16 KV cache, with the cross-chunk
-// combine done by the last CTA to finish (no second launch, no spinning).
+// GQA decode attention over the fp16 KV cache on the tensor cores
+// ("EdgeRunner Core Architecture" section 5.2: scores q.k / sqrt(hd), causal, a
+// query at position p attends rows 0..p, query head h reads KV head h / G;
+// softmax over the rows; o = sum p v).
 //
-// CTA (chunk c, KV head kvh, sequence b) scores the G = H / KV query heads of
-// the group against cache rows [c*CH, min((c+1)*CH, pos+1)) and keeps, per head,
-// the running max m, the running sum l = sum exp(s - m) and o = sum exp(s - m) v
-// (online softmax).  Rows of one head are contiguous ([head][position][dim]), so
-// the four warps stream consecutive rows with 128-bit loads, one iteration
-// ahead of the arithmetic.  Rows below `pos` were written by earlier steps, so
-// the first iteration's rows are requested before griddepcontrol.wait; only the
-// row at `pos` (written by the QKV kernel of this step) waits for it.  The CTA
-// that completes a (b, kvh) group last merges the chunks:
-//   M = max_c m_c,  o = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c
-// ("EdgeRunner Core Architecture" section 5.2: scale 1/sqrt(hd), causal, a
-// query at position p attends rows 0..p; query head h reads KV head h / G).
+// Work split.  The rows of every (sequence b, KV head) pair, rows 0..pos_b
+// each, form one list; warp w of the W warps of the grid takes the contiguous
+// range [w NR / W, (w+1) NR / W) (at least TA_MIN_ROWS rows per warp), so
+// every warp streams the same number of bytes whatever the positions.  A
+// warp keeps one online-softmax state (max m, sum l, o = sum e^(s - m) v, in
+// log2 units) per query head of the group for each (b, KV head) it touches.
+// A pair whose rows one warp covers is finished by that warp; otherwise each
+// covering warp leaves its state in global memory and the last one to arrive
+// (a counter per pair) merges them in warp order:
+//   M = max_w m_w,  o = sum_w e^(m_w - M) o_w / sum_w e^(m_w - M) l_w.
+//
+// Arithmetic per tile of 16 rows (mma.sync m16n8k16, fp32 accumulate):
+//   S^T = Q K^T: A = the group's queries, rows 0..7 the hi fp16 half of head
+//         g = row, rows 8..15 the lo half (q = hi + lo, exact to 2^-22 after
+//         a power-of-two rescale); B = K rows from shared memory (ldmatrix).
+//         Lane (g, t) ends up with head g's scores of rows 2t, 2t+1, 2t+8, 2t+9
+//         as hi + lo sums of its accumulator.
+//   O += P V: A = the probabilities in exactly that lane layout (hi rows 0..7,
+//         lo rows 8..15, p = hi + lo); B = V rows (ldmatrix.trans).
+// K and V tiles reach shared memory through cp.async (16 bytes per lane, rows
+// padded by 16 bytes so ldmatrix reads are free of bank conflicts), three
+// tiles per warp in flight.
 #include "common.cuh"
 #include "internal.h"
 
 namespace er {
 
-constexpr int AT_WARPS = 4;
-constexpr int AT_UNROLL = 4;
-constexpr int AT_COMBINE_SMEM = 48 * 1024;  // staging for the last CTA's merge
+constexpr int TA_WARPS = 8;
+constexpr int TA_SLOTS = 3;
+constexpr int TA_TILE = 16;
+constexpr int TA_MIN_ROWS = 64;  // rows per warp at least
+constexpr int TA_MAXB = 16;
 
 template <int HD>
-struct AtCfg {
-    static constexpr int LPR = HD / 8;    // lanes per row (8 halves each)
-    static constexpr int RPW = 32 / LPR;  // rows per warp step
-    static constexpr int RPI = AT_WARPS * RPW * AT_UNROLL;  // rows per CTA iteration
+struct TaCfg {
+    static constexpr int KC = HD / 16;                   // k16 chunks of a head (Q K^T)
+    static constexpr int NTD = HD / 8;                   // n8 tiles of a head (P V)
+    static constexpr int ROWB = HD * 2 + 16;             // padded row bytes in shared memory
+    static constexpr int TILEB = TA_TILE * ROWB;         // one K or V tile
+    static constexpr int SLOT = 2 * TILEB;               // K tile then V tile
+    static constexpr int CPL = TA_TILE * HD / 8 / 32;    // 16-byte chunks per lane per tile
+    static constexpr int SMEM = TA_WARPS * TA_SLOTS * SLOT;
 };
 
-__device__ inline void merge_state(float &m, float &l, float *acc, float m2, float l2, const float *acc2) {
-    float mn = fmaxf(m, m2);
-    if (mn == -INFINITY) return;
-    float c1 = exp2f(m - mn), c2 = exp2f(m2 - mn);
-    l = l * c1 + l2 * c2;
+ER_DEV void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+ER_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+ER_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+ER_DEV void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+ER_DEV void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+ER_DEV uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+struct TaGeom {
+    int NR, W;  // rows in the list, working warps
+    int T[TA_MAXB];
+    int base[TA_MAXB + 1];
+};
+
+__device__ inline void ta_locate(const TaGeom &g, int B, int u, int &b, int &kvh, int &seg_start, int &seg_end) {
+    b = 0;
+    while (b + 1 < B && u >= g.base[b + 1]) ++b;
+    kvh = (u - g.base[b]) / g.T[b];
+    seg_start = g.base[b] + kvh * g.T[b];
+    seg_end = seg_start + g.T[b];
+}
+
+// State of one warp for its piece of one (b, KV head): lane (g, t) holds head
+// g's running max (equal over t), a partial sum over its rows, and the hi/lo
+// accumulator tiles of O (dims 8j + 2t, 8j + 2t + 1).
+template <int HD>
+struct TaState {
+    float m, l;
+    float o[TaCfg<HD>::NTD][4];
+};
+
+// Rows [r0, r1) of the cache head at Kb / Vb (row-major [cap][HD]) for the G
+// query heads at qh (fp32 [G][HD], unscaled).
+template <int HD, int G>
+__device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, int r0, int r1, uint8_t *ring,
+                          int lane, TaState<HD> &st) {
+    using C = TaCfg<HD>;
+    const int g = lane >> 2, t = lane & 3;
+    // queries: scale to log2 units, rescale by a power of two so that the lo
+    // halves stay normal, split hi + lo into A fragments
+    const float qscale = 1.4426950408889634f / sqrtf((float)HD);
+    float qv[C::KC][4];
+    float qmax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = acc[i] * c1 + acc2[i] * c2;
-    m = mn;
+    for (int c = 0; c < C::KC; ++c) {
+        float2 x0 = make_float2(0.f, 0.f), x1 = x0;
+        if (g < G) {
+            x0 = __ldcg(reinterpret_cast<const float2 *>(qh + g * HD + 16 * c + 2 * t));
+            x1 = __ldcg(reinterpret_cast<const float2 *>(qh + g * HD + 16 * c + 2 * t + 8));
+        }
+        qv[c][0] = x0.x * qscale; qv[c][1] = x0.y * qscale; qv[c][2] = x1.x * qscale; qv[c][3] = x1.y * qscale;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qmax = fmaxf(qmax, fabsf(qv[c][i]));
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+    int e = 0;
+    if (qmax > 0.f && isfinite(qmax)) {
+        int E;
+        frexpf(qmax, &E);
+        e = 15 - E;
+    }
+    const float up = ldexpf(1.f, e), down = ldexpf(1.f, -e);
+    uint32_t qa[C::KC][4];
+#pragma unroll
+    for (int c = 0; c < C::KC; ++c) {
+        float hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float v = qv[c][i] * up;
+            hi[i] = __half2float(__float2half_rn(v));
+            lo[i] = v - hi[i];
+        }
+        qa[c][0] = pack_h2(hi[0], hi[1]);  // row g (hi), k = 2t, 2t+1
+        qa[c][1] = pack_h2(lo[0], lo[1]);  // row g + 8 (lo)
+        qa[c][2] = pack_h2(hi[2], hi[3]);  // row g, k = 2t + 8, 2t + 9
+        qa[c][3] = pack_h2(lo[2], lo[3]);
+    }
+
+    st.m = -INFINITY;
+    st.l = 0.f;
+#pragma unroll
+    for (int j = 0; j < C::NTD; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.f;
+
+    const int ntiles = (r1 - r0 + TA_TILE - 1) / TA_TILE;
+    const uint32_t ring_s = smem_u32(ring);
+    auto issue = [&](int k) {
+        if (k < ntiles) {
+            const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
+            const int rb = r0 + k * TA_TILE;
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i) {
+                const int ci = lane + 32 * i;            // chunk of the tile
+                const int row = ci / (HD / 8), col = ci % (HD / 8);
+                const bool ok = rb + row < r1;
+                const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 8;
+                const uint32_t d = (uint32_t)(row * C::ROWB + col * 16);
+                cp_async16(slot + d, Kb + off, ok ? 16u : 0u);
+                cp_async16(slot + C::TILEB + d, Vb + off, ok ? 16u : 0u);
+            }
+        }
+        cp_async_commit();  // an empty group keeps the count uniform
+    };
+    issue(0);
+    issue(1);
+    // ldmatrix row addresses of this lane (see the header): K as the B operand
+    // (rows (lane & 7) + 8 (lane >> 4), column half (lane >> 3) & 1), V
+    // transposed (rows (lane & 7) + 8 ((lane >> 3) & 1), column half lane >> 4)
+    const uint32_t k_lane = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB + ((lane >> 3) & 1) * 16);
+    const uint32_t v_lane = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB + (lane >> 4) * 16);
+    for (int k = 0; k < ntiles; ++k) {
+        issue(k + 2);
+        cp_async_wait<2>();
+        __syncwarp();
+        const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
+        // scores of 16 rows: two n8 tiles (rows 0..7 and 8..15 of the tile)
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < C::KC; ++c) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(slot + k_lane + c * 32, b0, b1, b2, b3);
+            mma_16816(s0, qa[c], b0, b1, s0);
+            mma_16816(s1, qa[c], b2, b3, s1);
+        }
+        const int rb = r0 + k * TA_TILE;
+        float sc[4] = {(s0[0] + s0[2]) * down, (s0[1] + s0[3]) * down, (s1[0] + s1[2]) * down,
+                       (s1[1] + s1[3]) * down};
+        const int rr[4] = {rb + 2 * t, rb + 2 * t + 1, rb + 2 * t + 8, rb + 2 * t + 9};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (rr[i] >= r1) sc[i] = -INFINITY;
+        float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+        const float mn = fmaxf(st.m, mt);
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mn != -INFINITY) {
+            if (mn != st.m) {
+                const float corr = exp2f(st.m - mn);
+                st.l *= corr;
+#pragma unroll
+                for (int j = 0; j < C::NTD; ++j) {
+                    st.o[j][0] *= corr; st.o[j][1] *= corr; st.o[j][2] *= corr; st.o[j][3] *= corr;
+                }
+                st.m = mn;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p[i] = exp2f(sc[i] - mn);
+            st.l += (p[0] + p[1]) + (p[2] + p[3]);
+        }
+        float ph[4], pl[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ph[i] = __half2float(__float2half_rn(p[i]));
+            pl[i] = p[i] - ph[i];
+        }
+        const uint32_t pa[4] = {pack_h2(ph[0], ph[1]), pack_h2(pl[0], pl[1]), pack_h2(ph[2], ph[3]),
+                                pack_h2(pl[2], pl[3])};
+#pragma unroll
+        for (int j2 = 0; j2 < C::NTD / 2; ++j2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(slot + v_lane + j2 * 32, b0, b1, b2, b3);
+            mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
+            mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
+        }
+        __syncwarp();  // every lane is done with this slot before it is refilled
+    }
+    cp_async_wait<0>();
+    // the row sum over the four lanes of the head
+    st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
+    st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
 }
 
 template <int HD, int G>
-__global__ void __launch_bounds__(AT_WARPS * 32) attn_kernel(const AttnArgs a) {
-    using C = AtCfg<HD>;
-    extern __shared__ float stage[];  // S * G * (HD + 2) floats, used by the last CTA
-    __shared__ float sm_m[AT_WARPS][G], sm_l[AT_WARPS][G];
-    __shared__ float sm_o[AT_WARPS][G][HD];
-    __shared__ int sm_last;
-
-    const int c = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+__global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArgs a) {
+    using C = TaCfg<HD>;
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rw = lane / C::LPR, dl = (lane % C::LPR) * 8;
-
-    // positions are inputs of the whole step: stable before the wait
-    const int pos = a.positions[b];
-    const int T = (pos >= 0 && pos < a.cap) ? pos + 1 : 0;
-    const int r0 = c * a.CH, r1 = min(r0 + a.CH, T);
-    const size_t head_off = (((size_t)b * a.L + a.layer) * a.KV + kvh) * (size_t)a.cap * HD;
-    const __half *Kb = a.kc + head_off + dl;
-    const __half *Vb = a.vc + head_off + dl;
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t *ring = smem + warp * TA_SLOTS * C::SLOT;
     const int qd = a.H * HD;
-    const int base0 = r0 + warp * C::RPW + rw;  // this lane's first row
-
-    uint4 kr[AT_UNROLL], vr[AT_UNROLL];
-#pragma unroll
-    for (int u = 0; u < AT_UNROLL; ++u) {
-        const int row = base0 + u * AT_WARPS * C::RPW;
-        kr[u] = vr[u] = make_uint4(0, 0, 0, 0);
-        if (row < r1 && row != pos) {
-            kr[u] = *reinterpret_cast<const uint4 *>(Kb + (size_t)row * HD);
-            vr[u] = *reinterpret_cast<const uint4 *>(Vb + (size_t)row * HD);
-        }
-    }
 
     pdl_wait();
     pdl_launch_dependents();
 
-#pragma unroll
-    for (int u = 0; u < AT_UNROLL; ++u) {
-        const int row = base0 + u * AT_WARPS * C::RPW;
-        if (row < r1 && row == pos) {
-            kr[u] = *reinterpret_cast<const uint4 *>(Kb + (size_t)row * HD);
-            vr[u] = *reinterpret_cast<const uint4 *>(Vb + (size_t)row * HD);
-        }
+    // geometry of the row list (positions are inputs of the step)
+    TaGeom geo;
+    geo.NR = 0;
+    for (int b = 0; b < a.B; ++b) {
+        const int pos = a.positions[b];
+        geo.T[b] = (pos >= 0 && pos < a.cap) ? pos + 1 : 0;
+        geo.base[b] = geo.NR;
+        geo.NR += a.KV * geo.T[b];
     }
+    geo.base[a.B] = geo.NR;
+    const int Wmax = gridDim.x * TA_WARPS;
+    geo.W = (geo.NR + TA_MIN_ROWS - 1) / TA_MIN_ROWS;
+    if (geo.W > Wmax) geo.W = Wmax;
+    const int w = blockIdx.x * TA_WARPS + warp;
+    if (w >= geo.W) return;
+    const int wa = (int)((long long)w * geo.NR / geo.W), wb = (int)((long long)(w + 1) * geo.NR / geo.W);
 
-    // q of the group, pre-scaled so scores are in log2 units
-    const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-    float qv[G][8];
+    int u = wa;
+    while (u < wb) {
+        int b, kvh, seg_start, seg_end;
+        ta_locate(geo, a.B, u, b, kvh, seg_start, seg_end);
+        const int r0 = u - seg_start, r1 = (wb < seg_end ? wb : seg_end) - seg_start;
+        const bool first_piece = u == wa;
+        u = wb < seg_end ? wb : seg_end;
+        const size_t head_off = (((size_t)b * a.L + a.layer) * a.KV + kvh) * (size_t)a.cap * HD;
+        TaState<HD> st;
+        ta_attend<HD, G>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, a.kc + head_off, a.vc + head_off, r0, r1, ring,
+                         lane, st);
+        float *o_grp = a.o + (size_t)b * qd + (size_t)kvh * G * HD;
+        if (seg_start >= wa && seg_end <= wb) {  // the whole pair: finish here
+            if (g < G) {
+                const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
 #pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-        const float4 *qp = reinterpret_cast<const float4 *>(a.q + (size_t)b * qd + (kvh * G + gi) * HD + dl);
-        float4 x0 = qp[0], x1 = qp[1];
-        qv[gi][0] = x0.x * qscale; qv[gi][1] = x0.y * qscale; qv[gi][2] = x0.z * qscale; qv[gi][3] = x0.w * qscale;
-        qv[gi][4] = x1.x * qscale; qv[gi][5] = x1.y * qscale; qv[gi][6] = x1.z * qscale; qv[gi][7] = x1.w * qscale;
-    }
-    float m[G], l[G], acc[G][8];
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-        m[gi] = -INFINITY;
-        l[gi] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[gi][i] = 0.f;
-    }
-
-    for (int base = base0; base - rw < r1; base += C::RPI) {
-        // next iteration's rows first, so their loads overlap this iteration's math
-        uint4 kn[AT_UNROLL], vn[AT_UNROLL];
-#pragma unroll
-        for (int u = 0; u < AT_UNROLL; ++u) {
-            const int row = base + C::RPI + u * AT_WARPS * C::RPW;
-            kn[u] = vn[u] = make_uint4(0, 0, 0, 0);
-            if (row < r1) {
-                kn[u] = *reinterpret_cast<const uint4 *>(Kb + (size_t)row * HD);
-                vn[u] = *reinterpret_cast<const uint4 *>(Vb + (size_t)row * HD);
+                for (int j = 0; j < C::NTD; ++j)
+                    *reinterpret_cast<float2 *>(o_grp + g * HD + 8 * j + 2 * t) =
+                        make_float2((st.o[j][0] + st.o[j][2]) * inv, (st.o[j][1] + st.o[j][3]) * inv);
             }
+            continue;
         }
-        float s[AT_UNROLL][G];
+        // shared with other warps: leave the state [G][m, l, -, -, o[HD]]
+        float *ps = a.part + ((size_t)w * 2 + (first_piece ? 0 : 1)) * G * (HD + 4);
+        if (g < G) {
+            if (t == 0) *reinterpret_cast<float2 *>(ps + g * (HD + 4)) = make_float2(st.m, st.l);
 #pragma unroll
-        for (int u = 0; u < AT_UNROLL; ++u) {
-            const bool ok = base + u * AT_WARPS * C::RPW < r1;
-            const __half2 *kh = reinterpret_cast<const __half2 *>(&kr[u]);
-            float kf[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float2 f = __half22float2(kh[i]);
-                kf[2 * i] = f.x;
-                kf[2 * i + 1] = f.y;
-            }
-#pragma unroll
-            for (int gi = 0; gi < G; ++gi) {
-                float d = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) d = fmaf(qv[gi][i], kf[i], d);
-#pragma unroll
-                for (int off = 1; off < C::LPR; off <<= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-                s[u][gi] = ok ? d : -INFINITY;
-            }
+            for (int j = 0; j < C::NTD; ++j)
+                *reinterpret_cast<float2 *>(ps + g * (HD + 4) + 4 + 8 * j + 2 * t) =
+                    make_float2(st.o[j][0] + st.o[j][2], st.o[j][1] + st.o[j][3]);
         }
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            float mn = m[gi];
-#pragma unroll
-            for (int u = 0; u < AT_UNROLL; ++u) mn = fmaxf(mn, s[u][gi]);
-            if (mn == -INFINITY) continue;
-            const float corr = exp2f(m[gi] - mn);
-            l[gi] *= corr;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[gi][i] *= corr;
-            m[gi] = mn;
-#pragma unroll
-            for (int u = 0; u < AT_UNROLL; ++u) {
-                const float p = exp2f(s[u][gi] - mn);
-                l[gi] += p;
-                const __half2 *vh = reinterpret_cast<const __half2 *>(&vr[u]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    float2 f = __half22float2(vh[i]);
-                    acc[gi][2 * i] = fmaf(p, f.x, acc[gi][2 * i]);
-                    acc[gi][2 * i + 1] = fmaf(p, f.y, acc[gi][2 * i + 1]);
+        __syncwarp();
+        const int grp = b * a.KV + kvh;
+        int last = 0;
+        if (lane == 0) last = atom_add_acq_rel_gpu(a.cnt + grp, 1);  // releases this warp's state
+        last = __shfl_sync(0xffffffffu, last, 0);
+        const int w_first = (int)(((long long)(seg_start + 1) * geo.W - 1) / geo.NR);
+        const int w_last = (int)(((long long)seg_end * geo.W - 1) / geo.NR);
+        if (last != w_last - w_first) continue;
+        __syncwarp();
+        // the last warp of the pair: merge the covering warps' states in warp
+        // order; each lane owns float4 chunks of the group's output (one head
+        // per chunk) and keeps every contributor's loads in flight together
+        const int s0 = ((long long)w_first * geo.NR / geo.W >= seg_start) ? 0 : 1;
+        auto state = [&](int ww) {
+            return a.part + ((size_t)ww * 2 + (ww == w_first ? s0 : 0)) * G * (HD + 4);
+        };
+        for (int ch = lane; ch < G * HD / 4; ch += 32) {
+            const int gi = (4 * ch) / HD, d = 4 * ch - gi * HD;
+            float M = -INFINITY;
+#pragma unroll 4
+            for (int ww = w_first; ww <= w_last; ++ww) M = fmaxf(M, __ldcg(state(ww) + gi * (HD + 4)));
+            float L = 0.f;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -INFINITY) {
+#pragma unroll 4
+                for (int ww = w_first; ww <= w_last; ++ww) {
+                    const float *q = state(ww) + gi * (HD + 4);
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(q));
+                    const float4 ov = __ldcg(reinterpret_cast<const float4 *>(q + 4 + d));
+                    const float ew = exp2f(ml.x - M);
+                    L = fmaf(ml.y, ew, L);
+                    O.x = fmaf(ov.x, ew, O.x); O.y = fmaf(ov.y, ew, O.y);
+                    O.z = fmaf(ov.z, ew, O.z); O.w = fmaf(ov.w, ew, O.w);
                 }
             }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            *reinterpret_cast<float4 *>(o_grp + gi * HD + d) = make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
         }
-#pragma unroll
-        for (int u = 0; u < AT_UNROLL; ++u) {
-            kr[u] = kn[u];
-            vr[u] = vn[u];
-        }
+        if (lane == 0) a.cnt[grp] = 0;
     }
-
-    // merge the RPW row slots of the warp (lanes with the same dl)
-#pragma unroll
-    for (int off = C::LPR; off < 32; off <<= 1) {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            float m2 = __shfl_xor_sync(0xffffffffu, m[gi], off);
-            float l2 = __shfl_xor_sync(0xffffffffu, l[gi], off);
-            float a2[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a2[i] = __shfl_xor_sync(0xffffffffu, acc[gi][i], off);
-            merge_state(m[gi], l[gi], acc[gi], m2, l2, a2);
-        }
-    }
-    if (rw == 0) {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            if (dl == 0) {
-                sm_m[warp][gi] = m[gi];
-                sm_l[warp][gi] = l[gi];
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sm_o[warp][gi][dl + i] = acc[gi][i];
-        }
-    }
-    __syncthreads();
-
-    // CTA partial -> scratch: per (b, kvh, c, gi): [m, l, o[HD]]
-    const int group = b * a.KV + kvh;
-    float *part = a.part + ((size_t)group * a.S + c) * G * (HD + 2);
-    for (int idx = tid; idx < G * (HD + 2); idx += blockDim.x) {
-        const int gi = idx / (HD + 2), j = idx % (HD + 2);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < AT_WARPS; ++w) M = fmaxf(M, sm_m[w][gi]);
-        float v = (j == 0) ? M : 0.f;
-        if (j > 0 && M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < AT_WARPS; ++w) {
-                const float e = exp2f(sm_m[w][gi] - M);
-                v += (j == 1 ? sm_l[w][gi] : sm_o[w][gi][j - 2]) * e;
-            }
-        }
-        part[idx] = v;
-    }
-    __syncthreads();
-    if (tid == 0) sm_last = atom_add_acq_rel_gpu(a.cnt + group, 1) == a.S - 1;  // releases the CTA's partial
-    __syncthreads();
-    if (!sm_last) return;
-
-    // last CTA of the group: stage every chunk's partial, then merge in chunk order
-    const float *gp = a.part + (size_t)group * a.S * G * (HD + 2);
-    const int nf = a.S * G * (HD + 2);
-    for (int i = tid; i < nf; i += blockDim.x) stage[i] = __ldcg(gp + i);
-    __syncthreads();
-    for (int idx = tid; idx < G * HD; idx += blockDim.x) {
-        const int gi = idx / HD, d = idx % HD;
-        float M = -INFINITY;
-        for (int cc = 0; cc < a.S; ++cc) M = fmaxf(M, stage[(cc * G + gi) * (HD + 2)]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-            for (int cc = 0; cc < a.S; ++cc) {
-                const float *pc = stage + (cc * G + gi) * (HD + 2);
-                const float e = exp2f(pc[0] - M);
-                L += pc[1] * e;
-                O += pc[2 + d] * e;
-            }
-        }
-        a.o[(size_t)b * qd + (kvh * G + gi) * HD + d] = (L > 0.f) ? O / L : 0.f;
-    }
-    if (tid == 0) a.cnt[group] = 0;
 }
 
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH) {
-    const int per_iter = AT_WARPS * (32 / (hd / 8)) * AT_UNROLL;  // rows one CTA covers per loop pass
-    long long groups = (long long)KV * B;
-    long long want = (4LL * num_sms + groups - 1) / groups;  // ~4 CTAs per SM
-    long long max_chunks = (cap + per_iter - 1) / per_iter;
-    long long s = want < max_chunks ? want : max_chunks;
-    // the last CTA stages every chunk's partial in shared memory (G <= 8)
-    const long long fit = AT_COMBINE_SMEM / (8LL * (hd + 2) * 4);
-    if (s > fit) s = fit;
-    if (s < 1) s = 1;
-    int ch = (int)((cap + s - 1) / s);
-    ch = (ch + per_iter - 1) / per_iter * per_iter;
-    *CH = ch;
-    *S = (cap + ch - 1) / ch;
+    (void)hd; (void)KV; (void)B; (void)cap;
+    *S = num_sms;        // CTAs of the launch (the kernel uses fewer for short lists)
+    *CH = TA_MIN_ROWS;   // rows per warp at least
 }
+
+size_t attention_part_floats(int hd, int G, int num_sms) { return (size_t)num_sms * TA_WARPS * 2 * G * (hd + 4); }
 
 template <int HD, int G>
 static cudaError_t at_launch(const AttnArgs &a, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(a.S, a.KV, a.B);
-    cfg.blockDim = dim3(AT_WARPS * 32);
-    cfg.dynamicSmemBytes = (size_t)a.S * G * (HD + 2) * sizeof(float);
+    cfg.gridDim = dim3((unsigned)a.S);
+    cfg.blockDim = dim3(TA_WARPS * 32);
+    cfg.dynamicSmemBytes = TaCfg<HD>::SMEM;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<HD, G>, a);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, G>, a);
 }
 
 template <int HD>
@@ -288,8 +376,12 @@ static cudaError_t at_launch_g(const AttnArgs &a, cudaStream_t st, bool pdl) {
 
 template <int HD, int G>
 static cudaError_t at_attr() {
-    return cudaFuncSetAttribute(attn_kernel<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                cudaSharedmemCarveoutMaxShared);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TaCfg<HD>::SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    return e;
 }
 
 cudaError_t attention_prepare() {
@@ -303,7 +395,7 @@ cudaError_t attention_prepare() {
 }
 
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl) {
-    if ((size_t)a.S * (a.H / a.KV) * (a.hd + 2) * sizeof(float) > AT_COMBINE_SMEM) return cudaErrorInvalidValue;
+    if (a.B > TA_MAXB || a.S < 1) return cudaErrorInvalidValue;
     if (a.hd == 64) return at_launch_g<64>(a, st, pdl);
     if (a.hd == 128) return at_launch_g<128>(a, st, pdl);
     return cudaErrorInvalidValue;
