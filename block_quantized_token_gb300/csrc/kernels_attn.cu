@@ -24,14 +24,14 @@
 //         lo rows 8..15, p = hi + lo); B = V rows (ldmatrix.trans).
 // K and V tiles reach shared memory through cp.async (16 bytes per lane, rows
 // padded by 16 bytes so ldmatrix reads are free of bank conflicts), three
-// tiles per warp in flight.
+// tiles per warp in flight while a fourth is consumed.
 #include "common.cuh"
 #include "internal.h"
 
 namespace er {
 
-constexpr int TA_WARPS = 8;
-constexpr int TA_SLOTS = 3;
+constexpr int TA_WARPS = 6;
+constexpr int TA_SLOTS = 4;
 constexpr int TA_TILE = 16;
 constexpr int TA_MIN_ROWS = 64;  // rows per warp at least
 constexpr int TA_MAXB = 16;
@@ -164,16 +164,15 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
         }
         cp_async_commit();  // an empty group keeps the count uniform
     };
-    issue(0);
-    issue(1);
+    for (int k = 0; k < TA_SLOTS - 1; ++k) issue(k);
     // ldmatrix row addresses of this lane (see the header): K as the B operand
     // (rows (lane & 7) + 8 (lane >> 4), column half (lane >> 3) & 1), V
     // transposed (rows (lane & 7) + 8 ((lane >> 3) & 1), column half lane >> 4)
     const uint32_t k_lane = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB + ((lane >> 3) & 1) * 16);
     const uint32_t v_lane = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB + (lane >> 4) * 16);
     for (int k = 0; k < ntiles; ++k) {
-        issue(k + 2);
-        cp_async_wait<2>();
+        issue(k + TA_SLOTS - 1);
+        cp_async_wait<TA_SLOTS - 1>();
         __syncwarp();
         const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
         // scores of 16 rows: two n8 tiles (rows 0..7 and 8..15 of the tile)

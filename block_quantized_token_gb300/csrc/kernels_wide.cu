@@ -282,11 +282,10 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
             const uint32_t sb = smem_u32(ring + sidx * C::SLOT);
             for (int i = 0; i < cnt; ++i)
                 gw_unit<QT>(sb + i * C::UB, xop + (uint32_t)(2 * (u0 + i)) * GW_BLOCK_BYTES, lane, acc);
+            // every lane's reads of the slot have returned (their values fed the
+            // MMAs above) before lane 0 lets the next bulk copy overwrite it
             __syncwarp();
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                issue_next();
-            }
+            if (lane == 0) issue_next();
         }
         if (failed) break;
         float v2[GW_NT][2];
