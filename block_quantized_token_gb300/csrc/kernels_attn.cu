@@ -311,21 +311,39 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArg
         };
         for (int ch = lane; ch < G * HD / 4; ch += 32) {
             const int gi = (4 * ch) / HD, d = 4 * ch - gi * HD;
-            float M = -INFINITY;
-#pragma unroll 4
-            for (int ww = w_first; ww <= w_last; ++ww) M = fmaxf(M, __ldcg(state(ww) + gi * (HD + 4)));
-            float L = 0.f;
+            float M = -INFINITY, L = 0.f;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
-#pragma unroll 4
-                for (int ww = w_first; ww <= w_last; ++ww) {
-                    const float *q = state(ww) + gi * (HD + 4);
-                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(q));
-                    const float4 ov = __ldcg(reinterpret_cast<const float4 *>(q + 4 + d));
-                    const float ew = exp2f(ml.x - M);
-                    L = fmaf(ml.y, ew, L);
-                    O.x = fmaf(ov.x, ew, O.x); O.y = fmaf(ov.y, ew, O.y);
-                    O.z = fmaf(ov.z, ew, O.z); O.w = fmaf(ov.w, ew, O.w);
+            for (int w0 = w_first; w0 <= w_last; w0 += 8) {  // eight states in flight, online rescale
+                float mm[8], ll[8];
+                float4 ov[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int ww = w0 + j;
+                    mm[j] = -INFINITY;
+                    ll[j] = 0.f;
+                    ov[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (ww <= w_last) {
+                        const float *q = state(ww) + gi * (HD + 4);
+                        const float2 ml = __ldcg(reinterpret_cast<const float2 *>(q));
+                        mm[j] = ml.x;
+                        ll[j] = ml.y;
+                        ov[j] = __ldcg(reinterpret_cast<const float4 *>(q + 4 + d));
+                    }
+                }
+                float mc = M;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) mc = fmaxf(mc, mm[j]);
+                if (mc == -INFINITY) continue;
+                const float corr = exp2f(M - mc);
+                L *= corr;
+                O.x *= corr; O.y *= corr; O.z *= corr; O.w *= corr;
+                M = mc;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float ew = exp2f(mm[j] - mc);
+                    L = fmaf(ll[j], ew, L);
+                    O.x = fmaf(ov[j].x, ew, O.x); O.y = fmaf(ov[j].y, ew, O.y);
+                    O.z = fmaf(ov[j].z, ew, O.z); O.w = fmaf(ov[j].w, ew, O.w);
                 }
             }
             const float inv = L > 0.f ? 1.f / L : 0.f;

@@ -280,8 +280,14 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
             }
             const int u0 = sl * C::SU, cnt = min(C::SU, nu - u0);
             const uint32_t sb = smem_u32(ring + sidx * C::SLOT);
-            for (int i = 0; i < cnt; ++i)
-                gw_unit<QT>(sb + i * C::UB, xop + (uint32_t)(2 * (u0 + i)) * GW_BLOCK_BYTES, lane, acc);
+            if (cnt == C::SU) {  // full slot: units unrolled so their loads and MMAs overlap
+#pragma unroll
+                for (int i = 0; i < C::SU; ++i)
+                    gw_unit<QT>(sb + i * C::UB, xop + (uint32_t)(2 * (u0 + i)) * GW_BLOCK_BYTES, lane, acc);
+            } else {
+                for (int i = 0; i < cnt; ++i)
+                    gw_unit<QT>(sb + i * C::UB, xop + (uint32_t)(2 * (u0 + i)) * GW_BLOCK_BYTES, lane, acc);
+            }
             // every lane's reads of the slot have returned (their values fed the
             // MMAs above) before lane 0 lets the next bulk copy overwrite it
             __syncwarp();
