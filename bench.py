@@ -70,6 +70,31 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+# DRAM bytes per launch of the dominant kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by workload and by a hash of the CUDA sources it was taken on: a
+# changed kernel reports no traffic until it is captured again.
+KERNEL_TRAFFIC = {
+    # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --steps 4 --warmup 3 --no-cpu-baseline`
+    "smollm_q8": ("19cac60d1585f37b", 190641152 + 3227648),
+}
+
+
+def csrc_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_quantized_token_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(workload: str):
+    e = KERNEL_TRAFFIC.get(workload)
+    return e[1] if e and e[0] == csrc_hash() else None
+
+
 def max_over_ranks(value: float, device) -> float:
     """Largest value over the ranks of the default process group (the value itself without one)."""
     import torch
@@ -256,7 +281,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             launch_ms = float(np.mean(graph_ms))
             achieved = bytes_step / (launch_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "kernel": "step_kernel", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": kernel_traffic(wl.name),
                     "peak_source": f"{peaks['source']} hbm_gbs (STREAM-style copy)",
                     "bytes_per_launch": bytes_step, "us_per_launch": launch_ms * 1e3,
                     "timing": "CUDA events around each step graph inside the timed region"}
@@ -397,6 +422,45 @@ def oracle_sample(wl: synth.Workload, steps: int, budget_s: float, seqs=None) ->
                f"({per:.1f} s/step)"}
 
 
+def gemv_sweep(reps: int = 50) -> dict:
+    """The isolated Q4_0 GEMV sweep of the 135M-shaped Q4_0 workload: M x K = 576x576, 1536x576, 49152x576,
+    batch 1, through er_matrix_gemv.  Each launch follows a 256 MiB write (larger than L2), so the weights come
+    from HBM; CUDA events around each launch on the launching stream."""
+    import torch
+    from block_quantized_token_gb300 import build as libbuild
+    if not libbuild.up_to_date():
+        libbuild.build()
+    from block_quantized_token_gb300 import er
+    peaks = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    out = {}
+    for rows, cols in ((576, 576), (1536, 576), (49152, 576)):
+        rng = np.random.default_rng(rows)
+        raw = synth.quantize((0.02 * rng.standard_normal((rows, cols))).astype(np.float32), "q4_0")
+        dev = torch.from_numpy(raw).cuda()
+        m = er.er_matrix_create(er.DTYPES["q4_0"], rows, cols, dev.data_ptr())
+        x = torch.from_numpy(rng.standard_normal((1, cols)).astype(np.float32)).cuda()
+        y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+        tot = 0.0
+        with torch.cuda.stream(stream):
+            for i in range(reps + 3):
+                flush.fill_(i & 0xFF)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                er.er_matrix_gemv(m, x.data_ptr(), 1, y.data_ptr(), stream.cuda_stream)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 3:
+                    tot += e0.elapsed_time(e1)
+        er.er_matrix_destroy(m)
+        us = tot / reps * 1e3
+        nbytes = rows * cols // 32 * 18 + cols * 4 + rows * 4
+        out[f"{rows}x{cols}"] = {"us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1),
+                                 "frac": round(nbytes / us / 1e3 / peaks["hbm_gbs"], 4)}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,6 +468,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="smollm_q8", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--gemv-sweep", action="store_true",
+                    help="time the isolated Q4_0 GEMV sweep (576x576, 1536x576, 49152x576) and print it")
     ap.add_argument("--schedule", default="auto", choices=["auto", "persistent", "kernels"],
                     help="step schedule (auto: the persistent kernel where the shape allows it)")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
@@ -411,6 +477,11 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller cases for profiling; not a bench workload)")
     args = ap.parse_args()
+
+    if args.gemv_sweep:
+        print(json.dumps({"gemv_sweep_q4_0": gemv_sweep(), "unit": "us per launch, algorithmic GB/s",
+                          "peak_gbs": measured_peaks()["hbm_gbs"]}))
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
