@@ -520,7 +520,7 @@ def main():
         if args.no_cpu_baseline:
             res["cpu_baseline"] = None
         else:
-            tps, done, info = oracle_sample(wl, 8, args.cpu_budget, seqs=[0])
+            tps, done, info = oracle_sample(wl, 64, args.cpu_budget, seqs=[0])
             res["cpu_baseline"] = {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle",
                                    "sample": f"sequence 0 from position {wl.prefill}: {info['how']} "
                                              f"({info['seconds']:.1f} s timed, numpy float64, BLAS on all cores)"}
