@@ -99,12 +99,14 @@ struct AttnArgs {
     const __half *kc, *vc;
     const int32_t *positions;
     float *o;  // [B][qd]
-    float *part;
-    int *cnt;
+    float *part;  // warp states of pairs shared by warps (attention_part_floats)
+    int *cnt;     // [B * KV] arrival counters (zero between launches)
     int *flags;
+    // S: CTAs of the launch; CH: rows per warp at least (both from attention_plan)
     int B, H, KV, hd, L, layer, cap, S, CH;
 };
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl);
+// launch shape of the attention kernel for a cache of this shape
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH);
 size_t attention_part_floats(int hd, int G, int num_sms);  // AttnArgs::part
 cudaError_t attention_prepare();  // kernel attributes (called by gemv_prepare)

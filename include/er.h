@@ -166,8 +166,10 @@ ER_API int32_t er_kv_get_schedule(const er_kv *kv);
 /* Kernel launches one er_decode_step enqueues under the schedule in effect
  * (memsets not counted), or -1 for NULL: 1 for the persistent schedule; for
  * the per-phase one, the embedding, per layer the QKV, attention, Wo, gate/up
- * and down launches (a GEMV takes one launch per group of at most 4 batch
- * columns that fit its shared memory), and the head. */
+ * and down launches, and the head.  A GEMV is one launch for batches up to 4
+ * and for batches of 5..16 whose matrices take the one-pass batched kernel
+ * (K a multiple of 64); otherwise one launch per group of at most 4 batch
+ * columns that fit its shared memory. */
 ER_API int32_t er_kv_launches_per_step(const er_kv *kv);
 
 /* positions_dev[b] += 1 for b < batch (chains steps without a host round trip). */
@@ -187,7 +189,7 @@ ER_API er_status er_get_device_error(er_kv *kv, int32_t *code, int32_t *non_fini
 typedef enum {
     ER_STAGE_EMBED = 0,   /* token row -> residual x                          */
     ER_STAGE_QKV = 1,     /* RMSNorm + [Wq;Wk;Wv] + RoPE + K/V append          */
-    ER_STAGE_ATTN = 2,    /* split-K GQA attention + combine                   */
+    ER_STAGE_ATTN = 2,    /* GQA attention (rows split over warps) + merges    */
     ER_STAGE_WO = 3,      /* Wo + residual                                     */
     ER_STAGE_GATEUP = 4,  /* RMSNorm + [Wgate;Wup] + SwiGLU                    */
     ER_STAGE_DOWN = 5,    /* Wdown + residual                                  */
