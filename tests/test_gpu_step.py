@@ -210,6 +210,36 @@ def test_small_models_ragged_batch(name, batch, schedule):
         s.close()
 
 
+WIDE_SHAPES = {
+    # K = 2048 and 2560 span 2 and 3 slices of the batched GEMV (the last one partial)
+    "q8_k2048": synth.ModelShape(n_layers=2, dim=2048, n_heads=16, n_kv_heads=4, head_dim=128, ffn_dim=2560,
+                                 vocab=1000, rope_base=10000.0, rms_eps=1e-5, w_type="q8_0", tied=False),
+    "q4_k2048_tied": synth.ModelShape(n_layers=2, dim=2048, n_heads=32, n_kv_heads=8, head_dim=64, ffn_dim=2560,
+                                      vocab=700, rope_base=500000.0, rms_eps=1e-6, w_type="q4_0", tied=True),
+}
+
+
+@pytest.mark.parametrize("name", list(WIDE_SHAPES))
+@pytest.mark.parametrize("batch", [6, 16])
+def test_batched_gemv_multi_slice(name, batch):
+    """Batches of 5..16 on the per-phase schedule with matrices of several K-slices: logits of every sequence
+    against the oracle over 2 chained steps, sequences at different positions."""
+    shape = WIDE_SHAPES[name]
+    wl = synth.Workload("t", shape, batch=batch, steps=2, prefill=29)
+    s = Setup(wl, schedule=KERNELS)
+    try:
+        rng = np.random.default_rng(batch + shape.dim)
+        tokens = rng.integers(0, shape.vocab, batch)
+        positions = rng.integers(0, 30, batch)
+        fed, hist = gpu_chain(s.state, wl, 2, tokens0=tokens, positions0=positions)
+        ofed, ohist = oracle.greedy(s.om, s.ocache(), tokens, positions, 2)
+        np.testing.assert_array_equal(fed, ofed)
+        for st in range(2):
+            logits_close(hist[st], ohist[st])
+    finally:
+        s.close()
+
+
 def test_nonfinite_flag():
     """An infinite block scale in the head makes logits non-finite: flag set, argmax stays in range."""
     shape = SMALL_SHAPES["q8_mha"]
