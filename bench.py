@@ -168,8 +168,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     import torch
 
     from block_quantized_token_gb300 import build as libbuild
-    if rank == 0 or not libbuild.up_to_date():
-        libbuild.build()
+    if rank == 0 and not libbuild.up_to_date():
+        libbuild.build()  # one rank builds; the others wait for it below
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     from block_quantized_token_gb300 import er, runtime
 
     dev = torch.device("cuda", local_rank)
