@@ -70,28 +70,33 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-# DRAM bytes per launch of the dominant kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by workload and by a hash of the CUDA sources it was taken on: a
-# changed kernel reports no traffic until it is captured again.
+# DRAM bytes per launch of the step kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by workload and by a hash of the kernel's sources at the capture:
+# a changed kernel reports no traffic until it is captured again.
 KERNEL_TRAFFIC = {
     # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --steps 4 --warmup 3 --no-cpu-baseline`
-    "smollm_q8": ("6a9db00448ae3f48", 190641152 + 3227648),
+    "smollm_q8": ("bde98dc1bdc1c289", 190641152 + 3227648),
 }
 
 
-def csrc_hash() -> str:
-    """Hash of the library's CUDA/C++ sources with comments and blank space removed (a comment edit keeps it)."""
+# sources the persistent step kernel is compiled from
+STEP_KERNEL_SOURCES = ("common.cuh", "gemv_core.cuh", "internal.h", "kernels_step.cuh", "kernels_step_q4.cu",
+                       "kernels_step_q8.cu", "layout.cuh")
+
+
+def csrc_hash(files=STEP_KERNEL_SOURCES) -> str:
+    """Hash of the step kernel's sources (and the C ABI header) with comments and blank space removed."""
     import hashlib
     import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "block_quantized_token_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name)) as f:
-                src = f.read()
-            src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-            src = re.sub(r"//[^\n]*", " ", src)
-            h.update(name.encode() + b"\0" + " ".join(src.split()).encode())
+    paths = [os.path.join(d, f) for f in files] + [os.path.join(ROOT, "include", "er.h")]
+    for path in paths:
+        with open(path) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(os.path.basename(path).encode() + b"\0" + " ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

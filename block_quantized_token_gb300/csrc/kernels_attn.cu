@@ -22,15 +22,16 @@
 //         as hi + lo sums of its accumulator.
 //   O += P V: A = the probabilities in exactly that lane layout (hi rows 0..7,
 //         lo rows 8..15, p = hi + lo); B = V rows (ldmatrix.trans).
-// K and V tiles reach shared memory through cp.async (16 bytes per lane, rows
-// padded by 16 bytes so ldmatrix reads are free of bank conflicts), three
-// tiles per warp in flight while a fourth is consumed.
+// K and V tiles reach shared memory through cp.async, 16 bytes per lane; the
+// 16-byte chunk c of row r is stored at chunk c ^ (r & 7) of the row, so the
+// eight rows an ldmatrix reads together sit in eight different bank groups.
+// Three tiles per warp are in flight while a fourth is consumed.
 #include "common.cuh"
 #include "internal.h"
 
 namespace er {
 
-constexpr int TA_WARPS = 6;
+constexpr int TA_WARPS = 7;
 constexpr int TA_SLOTS = 4;
 constexpr int TA_TILE = 16;
 constexpr int TA_MIN_ROWS = 64;  // rows per warp at least
@@ -40,7 +41,7 @@ template <int HD>
 struct TaCfg {
     static constexpr int KC = HD / 16;                   // k16 chunks of a head (Q K^T)
     static constexpr int NTD = HD / 8;                   // n8 tiles of a head (P V)
-    static constexpr int ROWB = HD * 2 + 16;             // padded row bytes in shared memory
+    static constexpr int ROWB = HD * 2;                  // row bytes in shared memory (chunks swizzled)
     static constexpr int TILEB = TA_TILE * ROWB;         // one K or V tile
     static constexpr int SLOT = 2 * TILEB;               // K tile then V tile
     static constexpr int CPL = TA_TILE * HD / 8 / 32;    // 16-byte chunks per lane per tile
@@ -157,7 +158,7 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
                 const int row = ci / (HD / 8), col = ci % (HD / 8);
                 const bool ok = rb + row < r1;
                 const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 8;
-                const uint32_t d = (uint32_t)(row * C::ROWB + col * 16);
+                const uint32_t d = (uint32_t)(row * C::ROWB + (col ^ (row & 7)) * 16);
                 cp_async16(slot + d, Kb + off, ok ? 16u : 0u);
                 cp_async16(slot + C::TILEB + d, Vb + off, ok ? 16u : 0u);
             }
@@ -168,8 +169,10 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
     // ldmatrix row addresses of this lane (see the header): K as the B operand
     // (rows (lane & 7) + 8 (lane >> 4), column half (lane >> 3) & 1), V
     // transposed (rows (lane & 7) + 8 ((lane >> 3) & 1), column half lane >> 4)
-    const uint32_t k_lane = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB + ((lane >> 3) & 1) * 16);
-    const uint32_t v_lane = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB + (lane >> 4) * 16);
+    // (the row index mod 8 is lane & 7 in both; chunks are XOR-swizzled by it)
+    const int sw = lane & 7;
+    const uint32_t k_row = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB), k_half = (lane >> 3) & 1;
+    const uint32_t v_row = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB), v_half = lane >> 4;
     for (int k = 0; k < ntiles; ++k) {
         issue(k + TA_SLOTS - 1);
         cp_async_wait<TA_SLOTS - 1>();
@@ -180,7 +183,7 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
 #pragma unroll
         for (int c = 0; c < C::KC; ++c) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(slot + k_lane + c * 32, b0, b1, b2, b3);
+            ldsm_x4(slot + k_row + (((2 * c + k_half) ^ sw) << 4), b0, b1, b2, b3);
             mma_16816(s0, qa[c], b0, b1, s0);
             mma_16816(s1, qa[c], b2, b3, s1);
         }
@@ -221,7 +224,7 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
 #pragma unroll
         for (int j2 = 0; j2 < C::NTD / 2; ++j2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(slot + v_lane + j2 * 32, b0, b1, b2, b3);
+            ldsm_x4_t(slot + v_row + (((2 * j2 + v_half) ^ sw) << 4), b0, b1, b2, b3);
             mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
             mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
         }
