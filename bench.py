@@ -75,7 +75,7 @@ def measured_peaks() -> dict:
 # a changed kernel reports no traffic until it is captured again.
 KERNEL_TRAFFIC = {
     # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --steps 4 --warmup 3 --no-cpu-baseline`
-    "smollm_q8": ("bde98dc1bdc1c289", 190641152 + 3227648),
+    "smollm_q8": ("35d7ab1969b026e2", 190641152 + 3227648),
 }
 
 

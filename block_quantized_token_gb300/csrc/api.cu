@@ -272,7 +272,7 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
         bool ok = true;
         size_t part = 0, ssq = 0;
         auto need = [&](const er::Mat &w) {
-            ok = ok && gemv_wide_fits(w.qt, w.K, batch, m->num_sms);
+            ok = ok && gemv_wide_fits(w.qt, w.K, batch, m->num_sms) && gemv_tc_fits(w.qt, w.K, batch, m->num_sms);
             part = std::max(part, gemv_wide_part_floats(w.R, w.K));
             ssq = std::max(ssq, gemv_wide_ssq_floats(w.K));
         };
@@ -424,7 +424,7 @@ static cudaError_t gemv_all(er_kv *kv, int epi, GemvArgs a, cudaStream_t st, boo
     if (kv->wide_part) {
         a.b0 = 0;
         a.B = kv->B;
-        return launch_gemv_wide(epi, a, kv->wide_part, kv->wide_ssq, kv->m->num_sms, st, pdl);
+        return launch_gemv_wide(epi, a, kv->wide_part, kv->wide_ssq, kv->m->num_sms, st, pdl, kv->wide_variant);
     }
     int per = gemv_max_cols(a.qt, a.K);
     for (int b0 = 0; b0 < kv->B; b0 += per) {
@@ -664,6 +664,21 @@ er_status er_kv_set_schedule(er_kv *kv, int32_t schedule) {
 }
 
 int32_t er_kv_get_schedule(const er_kv *kv) { return kv ? kv->schedule : -1; }
+
+er_status er_kv_set_wide_gemv(er_kv *kv, int32_t variant) {
+    if (!kv) return fail(ER_EINVAL, "kv is NULL");
+    if (variant != ER_WIDE_AUTO && variant != ER_WIDE_MMA_SYNC && variant != ER_WIDE_TCGEN05)
+        return fail(ER_EINVAL, "bad batched GEMV variant");
+    static_assert((int)ER_WIDE_MMA_SYNC == (int)er::WIDE_MMA_SYNC && (int)ER_WIDE_TCGEN05 == (int)er::WIDE_TCGEN05,
+                  "variant codes");
+    if (variant != kv->wide_variant) {
+        ER_CUDA(cudaDeviceSynchronize());
+        for (auto &g : kv->graphs) cudaGraphExecDestroy(g.exec);
+        kv->graphs.clear();
+        kv->wide_variant = variant;
+    }
+    return ER_OK;
+}
 
 int32_t er_kv_launches_per_step(const er_kv *kv) {
     if (!kv) return -1;

@@ -80,8 +80,16 @@ cudaError_t launch_gemv(int epi, const GemvArgs &a, int num_sms, cudaStream_t st
 // The whole batch (up to 16 columns, b0 = 0) in one pass over the weights:
 // K-slices of 1024 columns, partials wpart (gemv_wide_part_floats), per-slice
 // sums of squares wssq (gemv_wide_ssq_floats), counters a.cnt [R] (zero).
+// variant: WIDE_AUTO (by matrix size, gemv_wide_uses_tc), WIDE_MMA_SYNC or
+// WIDE_TCGEN05 (kernels_wide_tc.cu).
+enum WideVariant : int { WIDE_AUTO = 0, WIDE_MMA_SYNC = 1, WIDE_TCGEN05 = 2 };
 cudaError_t launch_gemv_wide(int epi, const GemvArgs &a, float *wpart, float *wssq, int num_sms, cudaStream_t st,
-                             bool pdl);
+                             bool pdl, int variant);
+bool gemv_wide_uses_tc(int variant, int R, int UPR);
+cudaError_t launch_gemv_tc(int epi, const GemvArgs &a, float *wpart, float *wssq, int num_sms, cudaStream_t st,
+                           bool pdl);
+cudaError_t gemv_tc_prepare();
+bool gemv_tc_fits(int qt, int K, int B, int num_sms);
 cudaError_t gemv_wide_prepare();
 bool gemv_wide_fits(int qt, int K, int B, int num_sms);
 size_t gemv_wide_part_floats(int R, int K);
@@ -221,6 +229,7 @@ struct er_kv {
     float *gemv_part;
     int *gemv_cnt;
     float *wide_part, *wide_ssq;  // batched GEMV scratch (nullptr: column groups instead)
+    int wide_variant;             // er::WideVariant of the batched GEMV
     unsigned long long *amax;
     int *done;
     int *flags;

@@ -363,6 +363,7 @@ static cudaError_t gw_attr() {
 }
 
 cudaError_t gemv_wide_prepare() {
+    if (cudaError_t e = gemv_tc_prepare(); e != cudaSuccess) return e;
     cudaError_t r[10] = {gw_attr<Q8_0, EPI_STORE>(), gw_attr<Q8_0, EPI_RESID>(), gw_attr<Q8_0, EPI_QKV>(),
                          gw_attr<Q8_0, EPI_SWIGLU>(), gw_attr<Q8_0, EPI_LOGITS>(), gw_attr<Q4_0, EPI_STORE>(),
                          gw_attr<Q4_0, EPI_RESID>(), gw_attr<Q4_0, EPI_QKV>(), gw_attr<Q4_0, EPI_SWIGLU>(),
@@ -380,7 +381,9 @@ bool gemv_wide_fits(int qt, int K, int B, int num_sms) {
            (K / 64 >= GW_SLICE_UNITS ? 2 * GW_SLICE_UNITS * B : 2 * (K / 64) * B) <= GW_WARPS * 32;
 }
 
-size_t gemv_wide_part_floats(int R, int K) { return gw_slices(K / 64) > 1 ? (size_t)gw_slices(K / 64) * R * 256 : 0; }
+// both batched kernels: one 16 x 16 partial per slice and row group (the
+// tcgen05 kernel writes one even for a single slice)
+size_t gemv_wide_part_floats(int R, int K) { return (size_t)gw_slices(K / 64) * R * 256; }
 size_t gemv_wide_ssq_floats(int K) { return (size_t)gw_slices(K / 64) * 16; }
 
 template <int QT, int EPI>
@@ -398,8 +401,19 @@ static cudaError_t gw_launch(const GemvArgs &a, float *wpart, float *wssq, int n
     return cudaLaunchKernelEx(&cfg, gemv_wide_kernel<QT, EPI>, a, wpart, wssq);
 }
 
+// Which batched kernel: the tcgen05 one from 2^18 units (about 285 MB of Q8_0
+// weights) up, where a CTA's warpgroups each stream many full 128-row tiles;
+// below that its per-tile fixed costs (prologue, one stage handoff per unit,
+// the finisher's tail) outweigh the faster tensor cores, measured on GB300.
+bool gemv_wide_uses_tc(int variant, int R, int UPR) {
+    if (variant == WIDE_MMA_SYNC) return false;
+    if (variant == WIDE_TCGEN05) return true;
+    return (long long)R * UPR >= (1ll << 18);
+}
+
 cudaError_t launch_gemv_wide(int epi, const GemvArgs &a, float *wpart, float *wssq, int num_sms, cudaStream_t st,
-                             bool pdl) {
+                             bool pdl, int variant) {
+    if (gemv_wide_uses_tc(variant, a.R, a.UPR)) return launch_gemv_tc(epi, a, wpart, wssq, num_sms, st, pdl);
     if (!gemv_wide_fits(a.qt, a.K, a.B, num_sms) || a.b0 != 0) return cudaErrorInvalidValue;
     if (a.qt == Q8_0) {
         switch (epi) {

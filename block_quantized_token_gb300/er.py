@@ -19,6 +19,7 @@ ER_OK, ER_EINVAL, ER_ENOMEM, ER_ECUDA, ER_EUNSUPPORTED, ER_EDEVICE = range(6)
 ER_F32, ER_F16, ER_Q4_0, ER_Q8_0 = 0, 1, 2, 8
 DTYPES = {"f32": ER_F32, "f16": ER_F16, "q4_0": ER_Q4_0, "q8_0": ER_Q8_0}
 ER_SCHEDULE_AUTO, ER_SCHEDULE_PERSISTENT, ER_SCHEDULE_KERNELS = 0, 1, 2
+ER_WIDE_AUTO, ER_WIDE_MMA_SYNC, ER_WIDE_TCGEN05 = 0, 1, 2
 (ER_STAGE_EMBED, ER_STAGE_QKV, ER_STAGE_ATTN, ER_STAGE_WO, ER_STAGE_GATEUP, ER_STAGE_DOWN,
  ER_STAGE_HEAD) = range(7)
 
@@ -65,6 +66,7 @@ def _load() -> ctypes.CDLL:
         "er_positions_increment": (I32, [VP, I32, VP]),
         "er_kv_set_schedule": (I32, [VP, I32]),
         "er_kv_get_schedule": (I32, [VP]),
+        "er_kv_set_wide_gemv": (I32, [VP, I32]),
         "er_kv_launches_per_step": (I32, [VP]),
         "er_get_device_error": (I32, [VP, P(I32), P(I32)]),
         "er_launch_stage": (I32, [VP, I32, I32, VP, VP, VP, VP, VP]),
@@ -86,7 +88,7 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_kv_create", "er_kv_destroy",
             "er_kv_layer_ptrs", "er_kv_write", "er_kv_read", "er_decode_step", "er_decode_step_eager", "er_positions_increment",
-            "er_kv_set_schedule", "er_kv_get_schedule",
+            "er_kv_set_schedule", "er_kv_get_schedule", "er_kv_set_wide_gemv",
             "er_get_device_error", "er_launch_stage", "er_matrix_create", "er_matrix_destroy",
             "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_kv_launches_per_step", "er_status_str", "er_last_error")
 
@@ -165,6 +167,10 @@ def er_positions_increment(positions: int, batch: int, stream: int = 0) -> None:
 
 def er_kv_set_schedule(kv: int, schedule: int) -> None:
     _check(_lib.er_kv_set_schedule(kv, schedule), "er_kv_set_schedule")
+
+
+def er_kv_set_wide_gemv(kv: int, variant: int) -> None:
+    _check(_lib.er_kv_set_wide_gemv(kv, variant), "er_kv_set_wide_gemv")
 
 
 def er_kv_get_schedule(kv: int) -> int:

@@ -110,6 +110,9 @@ class DecodeState:
     def set_schedule(self, schedule: int) -> None:
         er.er_kv_set_schedule(self.handle, schedule)
 
+    def set_wide_gemv(self, variant: int) -> None:
+        er.er_kv_set_wide_gemv(self.handle, variant)
+
     @property
     def schedule(self) -> int:
         return er.er_kv_get_schedule(self.handle)

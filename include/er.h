@@ -163,6 +163,18 @@ typedef enum { ER_SCHEDULE_AUTO = 0, ER_SCHEDULE_PERSISTENT = 1, ER_SCHEDULE_KER
 ER_API er_status er_kv_set_schedule(er_kv *kv, int32_t schedule);
 /* The schedule in effect (ER_SCHEDULE_PERSISTENT or ER_SCHEDULE_KERNELS), or -1 for NULL. */
 ER_API int32_t er_kv_get_schedule(const er_kv *kv);
+/* Which kernel runs the one-pass batched GEMV (batches of 5..16, per-phase
+ * schedule).  Both compute the same products and epilogues:
+ *   ER_WIDE_AUTO       by matrix size: the tcgen05 kernel for matrices of at
+ *                      least 2^18 units of 16 rows x 64 columns (such as an
+ *                      8B-class LM head), the mma.sync kernel below (default)
+ *   ER_WIDE_MMA_SYNC   warp-level mma.sync, weights dequantised in registers
+ *   ER_WIDE_TCGEN05    tcgen05.mma, weights dequantised into tensor memory,
+ *                      fp32 accumulators in tensor memory
+ * The choice drops kv's recorded graphs.  ER_EINVAL for another value; no
+ * effect on batches the batched GEMV does not take. */
+typedef enum { ER_WIDE_AUTO = 0, ER_WIDE_MMA_SYNC = 1, ER_WIDE_TCGEN05 = 2 } er_wide_gemv;
+ER_API er_status er_kv_set_wide_gemv(er_kv *kv, int32_t variant);
 /* Kernel launches one er_decode_step enqueues under the schedule in effect
  * (memsets not counted), or -1 for NULL: 1 for the persistent schedule; for
  * the per-phase one, the embedding, per layer the QKV, attention, Wo, gate/up

@@ -85,3 +85,6 @@ def test_null_arguments_rejected(er):
     with pytest.raises(er.ErError) as e:
         er.er_kv_create(0, 1, 16)
     assert e.value.status == er.ER_EINVAL
+    with pytest.raises(er.ErError) as e:
+        er.er_kv_set_wide_gemv(0, er.ER_WIDE_TCGEN05)
+    assert e.value.status == er.ER_EINVAL

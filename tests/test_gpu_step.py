@@ -219,15 +219,20 @@ WIDE_SHAPES = {
 }
 
 
+WIDE_VARIANTS = {"mma_sync": 1, "tcgen05": 2}  # er_wide_gemv: ER_WIDE_MMA_SYNC, ER_WIDE_TCGEN05
+
+
+@pytest.mark.parametrize("variant", list(WIDE_VARIANTS))
 @pytest.mark.parametrize("name", list(WIDE_SHAPES))
 @pytest.mark.parametrize("batch", [6, 16])
-def test_batched_gemv_multi_slice(name, batch):
-    """Batches of 5..16 on the per-phase schedule with matrices of several K-slices: logits of every sequence
-    against the oracle over 2 chained steps, sequences at different positions."""
+def test_batched_gemv_multi_slice(name, batch, variant):
+    """Batches of 5..16 on the per-phase schedule with matrices of several K-slices, under both batched GEMV
+    kernels: logits of every sequence against the oracle over 2 chained steps, sequences at different positions."""
     shape = WIDE_SHAPES[name]
     wl = synth.Workload("t", shape, batch=batch, steps=2, prefill=29)
     s = Setup(wl, schedule=KERNELS)
     try:
+        s.state.set_wide_gemv(WIDE_VARIANTS[variant])
         rng = np.random.default_rng(batch + shape.dim)
         tokens = rng.integers(0, shape.vocab, batch)
         positions = rng.integers(0, 30, batch)
@@ -236,6 +241,40 @@ def test_batched_gemv_multi_slice(name, batch):
         np.testing.assert_array_equal(fed, ofed)
         for st in range(2):
             logits_close(hist[st], ohist[st])
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("name", ["q4_tied_g2", "q8_mha", "q4_hd128_g4"])
+@pytest.mark.parametrize("batch", [5, 16])
+def test_small_models_tcgen05_batched_gemv(name, batch):
+    """The tcgen05 batched GEMV forced on small shapes (one K-slice, ragged 128-row tiles, tied Q4_0 heads):
+    greedy tokens and logits of 3 chained steps against the oracle."""
+    shape = SMALL_SHAPES[name]
+    wl = synth.Workload("t", shape, batch=batch, steps=3, prefill=37)
+    s = Setup(wl, schedule=KERNELS)
+    try:
+        s.state.set_wide_gemv(WIDE_VARIANTS["tcgen05"])
+        rng = np.random.default_rng(batch + 7)
+        tokens = rng.integers(0, shape.vocab, batch)
+        positions = rng.integers(0, 38, batch)
+        fed, hist = gpu_chain(s.state, wl, 3, tokens0=tokens, positions0=positions)
+        ofed, ohist = oracle.greedy(s.om, s.ocache(), tokens, positions, 3)
+        np.testing.assert_array_equal(fed, ofed)
+        for st in range(3):
+            logits_close(hist[st], ohist[st])
+    finally:
+        s.close()
+
+
+def test_wide_gemv_variant_rejected():
+    """An unknown batched GEMV variant is refused with ER_EINVAL."""
+    wl = synth.Workload("t", SMALL_SHAPES["q8_mha"], batch=6, steps=1, prefill=4)
+    s = Setup(wl, schedule=KERNELS)
+    try:
+        with pytest.raises(_er().ErError) as e:
+            s.state.set_wide_gemv(7)
+        assert e.value.status == _er().ER_EINVAL
     finally:
         s.close()
 
