@@ -25,14 +25,14 @@
 // K and V tiles reach shared memory through cp.async, 16 bytes per lane; the
 // 16-byte chunk c of row r is stored at chunk c ^ (r & 7) of the row, so the
 // eight rows an ldmatrix reads together sit in eight different bank groups.
-// Three tiles per warp are in flight while a fourth is consumed.
+// Two tiles per warp are in flight while a third is consumed.
 #include "common.cuh"
 #include "internal.h"
 
 namespace er {
 
-constexpr int TA_WARPS = 7;
-constexpr int TA_SLOTS = 4;
+constexpr int TA_WARPS = 8;
+constexpr int TA_SLOTS = 3;
 constexpr int TA_TILE = 16;
 constexpr int TA_MIN_ROWS = 64;  // rows per warp at least
 constexpr int TA_MAXB = 16;
