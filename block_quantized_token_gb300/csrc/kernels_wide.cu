@@ -16,7 +16,9 @@
 //
 // Operand: per CTA, once, for its slice: every column's elements of the slice
 // times the RMSNorm gain, scaled by one power of two per column (largest
-// element in [2^14, 2^15)) and split into hi + lo fp16.  The slice's sum of
+// element in [2^14, 2^15)) and split into hi + lo fp16, in the MMA's B
+// fragment order with each column's 16-byte chunks XOR-swizzled by the batch
+// column (conflict-free 128-bit stores while it is built).  The slice's sum of
 // squares of x per column goes to global memory for the finisher's 1/rms.
 #include "gemv_core.cuh"
 
@@ -238,16 +240,26 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
     if (item) {
         const float sc = 1.f / fac[b];
         uint8_t *area = op + kb * GW_BLOCK_BYTES + 2 * b * 64;
+        // 16-byte chunk tt of the column holds element pairs p = 8h + 4reg + tt as
+        // words 2h + reg; it is stored at chunk tt ^ (b & 3), so that the 16
+        // columns' stores of one chunk spread over the bank groups
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {  // element pair (2p, 2p+1) of the block
-            const int h = p >> 3, w8 = p & 7, reg = w8 >> 2, tt = w8 & 3;
-            const float v0 = v[2 * p] * sc, v1 = v[2 * p + 1] * sc;
-            const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-            const __half l0 = __float2half_rn(v0 - __half2float(h0));
-            const __half l1 = __float2half_rn(v1 - __half2float(h1));
-            const int off = tt * 16 + (h * 2 + reg) * 4;
-            *reinterpret_cast<__half2 *>(area + off) = __halves2half2(h0, h1);
-            *reinterpret_cast<__half2 *>(area + 64 + off) = __halves2half2(l0, l1);
+        for (int tt = 0; tt < 4; ++tt) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int p = (w >> 1) * 8 + (w & 1) * 4 + tt;  // element pair (2p, 2p+1) of the block
+                const float v0 = v[2 * p] * sc, v1 = v[2 * p + 1] * sc;
+                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+                const __half l0 = __float2half_rn(v0 - __half2float(h0));
+                const __half l1 = __float2half_rn(v1 - __half2float(h1));
+                const __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
+                hw[w] = *reinterpret_cast<const uint32_t *>(&hh);
+                lw[w] = *reinterpret_cast<const uint32_t *>(&ll);
+            }
+            const int co = (tt ^ (b & 3)) * 16;
+            *reinterpret_cast<uint4 *>(area + co) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(area + 64 + co) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
     }
     __syncthreads();
@@ -260,7 +272,8 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
 
     // ---- consume: whole row groups, slice units in order
     const int g = lane >> 2, t = lane & 3;
-    const uint32_t xop = smem_u32(op) + (uint32_t)(g * 64 + t * 16);
+    // column g of an n8 tile is batch column 4j + g / 2 (hi, lo): its chunk t sits at t ^ ((g / 2) & 3)
+    const uint32_t xop = smem_u32(op) + (uint32_t)(g * 64 + ((t ^ ((g >> 1) & 3)) * 16));
     float fj[GW_NT];
 #pragma unroll
     for (int jj = 0; jj < GW_NT; ++jj) fj[jj] = (4 * jj + t < a.B) ? fac[4 * jj + t] : 0.f;
