@@ -193,35 +193,48 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
             reinterpret_cast<uint32_t *>(op + kb * GW_BLOCK_BYTES + 2 * a.B * 64)[r] = 0u;
         }
     __syncthreads();
-    // one thread per (block, column): 32 elements of x, their gain, sum of squares and largest |x g|
-    const int kb = tid / a.B, b = tid - kb * a.B;
-    const bool item = kb < nbs;
-    float v[32];
-    float ssq = 0.f, m = 0.f;
-    if (item) {
-        const int k = ku0 * 64 + kb * 32;
-        const float4 *xp = reinterpret_cast<const float4 *>(a.x + (size_t)b * a.K + k);
+    // Warps read x in 512-byte segments of one column (lane l: elements 4l .. 4l + 3 of the segment),
+    // so every load instruction touches 4 cache lines.  The 8 lanes of one 32-element block reduce its
+    // sum of squares and largest |x g| by shuffles; lane 8i writes them.
+    const int nel = nu * 64, spc = (nel + 127) / 128, nseg = a.B * spc;  // segments per column, in all
+    float v[8][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 x4 = __ldcg(xp + i);
-            v[4 * i] = x4.x; v[4 * i + 1] = x4.y; v[4 * i + 2] = x4.z; v[4 * i + 3] = x4.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ssq = fmaf(v[i], v[i], ssq);
-        if (a.gain) {
-            const float4 *gp = reinterpret_cast<const float4 *>(a.gain + k);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 g4 = __ldg(gp + i);
-                v[4 * i] *= g4.x; v[4 * i + 1] *= g4.y; v[4 * i + 2] *= g4.z; v[4 * i + 3] *= g4.w;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-        if (!isfinite(m)) m = 0.f;
-        atomicMax(cmax + b, __float_as_uint(m));  // non-negative floats order as their bits
+    for (int i = 0; i < 8; ++i) {
+        const int seg = warp + GW_WARPS * i;
+        const int b = seg / spc, e0 = (seg - b * spc) * 128 + 4 * lane;  // element of the slice
+        const bool live = seg < nseg && e0 < nel;
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) x4 = __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.K + ku0 * 64 + e0));
+        v[i][0] = x4.x; v[i][1] = x4.y; v[i][2] = x4.z; v[i][3] = x4.w;
     }
-    issq[tid] = ssq;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int seg = warp + GW_WARPS * i;
+        if (seg >= nseg) break;  // warp-uniform
+        const int b = seg / spc, e0 = (seg - b * spc) * 128 + 4 * lane;
+        const bool live = e0 < nel;
+        float ssq = 0.f, m = 0.f;
+        if (live) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ssq = fmaf(v[i][c], v[i][c], ssq);
+            if (a.gain) {
+                const float4 g4 = __ldg(reinterpret_cast<const float4 *>(a.gain + ku0 * 64 + e0));
+                v[i][0] *= g4.x; v[i][1] *= g4.y; v[i][2] *= g4.z; v[i][3] *= g4.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) m = fmaxf(m, fabsf(v[i][c]));
+        }
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) {
+            ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        }
+        if (live && (lane & 7) == 0) {
+            issq[(e0 >> 5) * a.B + b] = ssq;
+            if (!isfinite(m)) m = 0.f;
+            atomicMax(cmax + b, __float_as_uint(m));  // non-negative floats order as their bits
+        }
+    }
     __syncthreads();
     if (tid < a.B) {
         float t = 0.f;
@@ -237,29 +250,26 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
         fac[tid] = ldexpf(1.f, -e);
     }
     __syncthreads();
-    if (item) {
+    // hi/lo split of each lane's two element pairs; pair p = 8h + 4reg + tt of a block is word 2h + reg of
+    // 16-byte chunk tt of the column, stored at chunk tt ^ (b & 3)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int seg = warp + GW_WARPS * i;
+        if (seg >= nseg) break;
+        const int b = seg / spc, e0 = (seg - b * spc) * 128 + 4 * lane;
+        if (e0 >= nel) continue;
         const float sc = 1.f / fac[b];
-        uint8_t *area = op + kb * GW_BLOCK_BYTES + 2 * b * 64;
-        // 16-byte chunk tt of the column holds element pairs p = 8h + 4reg + tt as
-        // words 2h + reg; it is stored at chunk tt ^ (b & 3), so that the 16
-        // columns' stores of one chunk spread over the bank groups
+        uint8_t *area = op + (e0 >> 5) * GW_BLOCK_BYTES + 2 * b * 64;
 #pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const int p = (w >> 1) * 8 + (w & 1) * 4 + tt;  // element pair (2p, 2p+1) of the block
-                const float v0 = v[2 * p] * sc, v1 = v[2 * p + 1] * sc;
-                const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-                const __half l0 = __float2half_rn(v0 - __half2float(h0));
-                const __half l1 = __float2half_rn(v1 - __half2float(h1));
-                const __half2 hh = __halves2half2(h0, h1), ll = __halves2half2(l0, l1);
-                hw[w] = *reinterpret_cast<const uint32_t *>(&hh);
-                lw[w] = *reinterpret_cast<const uint32_t *>(&ll);
-            }
-            const int co = (tt ^ (b & 3)) * 16;
-            *reinterpret_cast<uint4 *>(area + co) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(area + 64 + co) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        for (int q = 0; q < 2; ++q) {
+            const int p = ((e0 & 31) >> 1) + q;
+            const int off = (((p & 3) ^ (b & 3)) << 4) + ((((p >> 3) << 1) | ((p >> 2) & 1)) << 2);
+            const float v0 = v[i][2 * q] * sc, v1 = v[i][2 * q + 1] * sc;
+            const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+            const __half l0 = __float2half_rn(v0 - __half2float(h0));
+            const __half l1 = __float2half_rn(v1 - __half2float(h1));
+            *reinterpret_cast<__half2 *>(area + off) = __halves2half2(h0, h1);
+            *reinterpret_cast<__half2 *>(area + 64 + off) = __halves2half2(l0, l1);
         }
     }
     __syncthreads();
