@@ -288,7 +288,8 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
 #pragma unroll
     for (int jj = 0; jj < GW_NT; ++jj) fj[jj] = (4 * jj + t < a.B) ? fac[4 * jj + t] : 0.f;
     int k = 0;  // ring slot counter
-    bool failed = false;
+    bool failed = false, fready = false;
+    float f[GW_NT];
     for (int it = 0; it < my_items && !failed; ++it) {
         const int rg = rg0 + warp + GW_WARPS * it;
         float acc[GW_NT][2];
@@ -337,25 +338,40 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
             if (old != S - 1) continue;
 #pragma unroll
             for (int jj = 0; jj < GW_NT; ++jj) v2[jj][0] = v2[jj][1] = 0.f;
-            for (int ss = 0; ss < S; ++ss) {
-                const float4 *qp = reinterpret_cast<const float4 *>(wpart + ((size_t)ss * a.R + rg) * 256 + lane * 8);
-                const float4 p0 = __ldcg(qp), p1 = __ldcg(qp + 1);
-                v2[0][0] += p0.x; v2[0][1] += p0.y; v2[1][0] += p0.z; v2[1][1] += p0.w;
-                v2[2][0] += p1.x; v2[2][1] += p1.y; v2[3][0] += p1.z; v2[3][1] += p1.w;
+            for (int s0 = 0; s0 < S; s0 += 4) {  // 4 slices' loads in flight, added in slice order
+                float4 pv[4][2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (s0 + i < S) {
+                        const float4 *qp =
+                            reinterpret_cast<const float4 *>(wpart + ((size_t)(s0 + i) * a.R + rg) * 256 + lane * 8);
+                        pv[i][0] = __ldcg(qp);
+                        pv[i][1] = __ldcg(qp + 1);
+                    }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (s0 + i < S) {
+                        const float4 p0 = pv[i][0], p1 = pv[i][1];
+                        v2[0][0] += p0.x; v2[0][1] += p0.y; v2[1][0] += p0.z; v2[1][1] += p0.w;
+                        v2[2][0] += p1.x; v2[2][1] += p1.y; v2[3][0] += p1.z; v2[3][1] += p1.w;
+                    }
             }
             if (lane == 0) a.cnt[rg] = 0;
         }
-        // 1/rms of each of this lane's columns, from the slices' sums of squares (slice order)
-        float f[GW_NT];
+        // 1/rms of each of this lane's columns, from the slices' sums of squares (slice order), once per
+        // warp: every slice's CTA wrote its sums before the partials this warp has acquired
+        if (!fready) {
 #pragma unroll
-        for (int jj = 0; jj < GW_NT; ++jj) {
-            f[jj] = 1.f;
-            const int bb = 4 * jj + t;
-            if (a.gain && bb < a.B) {
-                float t2 = 0.f;
-                for (int ss = 0; ss < S; ++ss) t2 += __ldcg(wssq + ss * 16 + bb);
-                f[jj] = 1.f / sqrtf(t2 / (float)a.K + a.eps);
+            for (int jj = 0; jj < GW_NT; ++jj) {
+                f[jj] = 1.f;
+                const int bb = 4 * jj + t;
+                if (a.gain && bb < a.B) {
+                    float t2 = 0.f;
+                    for (int ss = 0; ss < S; ++ss) t2 += __ldcg(wssq + ss * 16 + bb);
+                    f[jj] = 1.f / sqrtf(t2 / (float)a.K + a.eps);
+                }
             }
+            fready = true;
         }
         if (EPI == EPI_LOGITS) {
             gw_logits(a, rg, v2, f, lane);
