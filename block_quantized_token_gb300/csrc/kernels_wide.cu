@@ -183,7 +183,9 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
 
     // ---- everything above touches only constant weights; now wait for inputs
     pdl_wait();
-    if (tid == 0) stop_s = *reinterpret_cast<volatile int *>(a.flags) & ER_FLAG_WAIT;
+    // an earlier kernel's give-up flag, read now and published after the operand build, so that
+    // nothing waits for this load before then
+    const int stop_r = tid == 0 ? (*reinterpret_cast<volatile int *>(a.flags) & ER_FLAG_WAIT) : 0;
     if (tid < 16) cmax[tid] = 0u;
     // zero the operand columns past the batch (their MMA results are never read, but must be finite)
     const int nbs = (nu * 64) / 32;  // blocks in this slice
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
             *reinterpret_cast<__half2 *>(area + 64 + off) = __halves2half2(l0, l1);
         }
     }
+    if (tid == 0) stop_s = stop_r;
     __syncthreads();
     if (stop_s) {  // an earlier kernel gave up on a wait: drain and stop
         if (lane == 0)

@@ -535,8 +535,10 @@ __global__ void __launch_bounds__(TW_THREADS, 1) gemv_tc_kernel(const GemvArgs a
     if (!producer) {
         pdl_wait();
         const int ot = tid - 32 * TW_WG;
-        if (ot == 0) *stop_s = *reinterpret_cast<volatile int *>(a.flags) & ER_FLAG_WAIT;
+        // an earlier kernel's give-up flag: published after the operand build, so nothing waits for it before
+        const int stop_r = ot == 0 ? (*reinterpret_cast<volatile int *>(a.flags) & ER_FLAG_WAIT) : 0;
         tw_operand(a, s, ku0, nu, opnd, fac, cmax, issq, wssq, ot);
+        if (ot == 0) *stop_s = stop_r;
     }
     __syncthreads();
     const bool stop = *stop_s != 0;  // an earlier kernel gave up on a wait: drain and stop
