@@ -116,28 +116,6 @@ ER_DEV void tc_wait_ld(uint32_t (&a)[32], uint32_t (&b)[32]) {
 ER_DEV void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-ER_DEV bool mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-ER_DEV bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
 ER_DEV unsigned ld_acquire_cta(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
@@ -491,7 +469,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) gemv_tc_kernel(const GemvArgs a
             }
             for (int k = 0; k < TW_NBUF; ++k) {
                 mbar_init(b + 2 * TW_NS + k, 4);            // afull: one arrival per row warp
-                mbar_init(b + 2 * TW_NS + TW_NBUF + k, 1);  // dfull: the control thread's commit
+                mbar_init(b + 2 * TW_NS + TW_NBUF + k, 1);  // dfull: the MMA warp's commit
             }
             tiles_done[i] = 0u;
         }
