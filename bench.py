@@ -38,20 +38,29 @@ BPB = {"q8_0": 34, "q4_0": 18}
 # ----------------------------------------------------------------------------------------------
 # algorithmic bytes (each weight byte once per step, KV rows read once, outputs written once)
 # ----------------------------------------------------------------------------------------------
+def matrix_bytes(s: synth.ModelShape) -> dict[str, float]:
+    """GGUF bytes of each GEMV's weights: one layer's fused Q/K/V, Wo, gate/up and down, and the head."""
+    bpb = BPB[s.w_type] / 32.0
+    D, qd, kvd, F, V = s.dim, s.qd, s.kvd, s.ffn_dim, s.vocab
+    return {"qkv": (qd + 2 * kvd) * D * bpb, "wo": D * qd * bpb, "gateup": 2 * F * D * bpb, "down": D * F * bpb,
+            "head": V * D * bpb}
+
+
 def stage_bytes(wl: synth.Workload, pos: np.ndarray) -> dict[str, float]:
     s = wl.shape
     bpb = BPB[s.w_type] / 32.0
     B = wl.batch
     D, qd, kvd, F, V = s.dim, s.qd, s.kvd, s.ffn_dim, s.vocab
+    w = matrix_bytes(s)
     attn_rows = float(np.sum(pos + 1))
     return {
         "embed": B * D * (2.0 if not s.tied else bpb) + B * D * 4,
-        "qkv": (qd + 2 * kvd) * D * bpb + B * (D * 4 + qd * 4 + 2 * kvd * 2) + D * 4,
+        "qkv": w["qkv"] + B * (D * 4 + qd * 4 + 2 * kvd * 2) + D * 4,
         "attn": attn_rows * kvd * 2 * 2 + B * qd * 4 * 2,
-        "wo": D * qd * bpb + B * (qd * 4 + 2 * D * 4),
-        "gateup": 2 * F * D * bpb + B * (D * 4 + F * 4) + D * 4,
-        "down": D * F * bpb + B * (F * 4 + 2 * D * 4),
-        "head": V * D * bpb + B * (D * 4 + V * 4) + D * 4,
+        "wo": w["wo"] + B * (qd * 4 + 2 * D * 4),
+        "gateup": w["gateup"] + B * (D * 4 + F * 4) + D * 4,
+        "down": w["down"] + B * (F * 4 + 2 * D * 4),
+        "head": w["head"] + B * (D * 4 + V * 4) + D * 4,
     }
 
 
