@@ -65,14 +65,22 @@ class OracleModel:
     `tensors` maps GGUF names ("blk.{l}.attn_q.weight", "token_embd.weight", ...)
     to stored arrays: float32 gains, float16 embedding, or uint8 block bytes.
     It may be a lazy mapping (only `__getitem__` is used).  With
-    `cache_dequant`, each dequantised matrix is kept after first use.
+    `cache_dequant`, each dequantised matrix is kept after first use, as
+    `cache_dtype`.  float32 halves the memory of a large model and loses
+    nothing: every dequantised value d * q has at most 19 significant bits
+    (an 11-bit fp16 significand times an integer of at most 8 bits), and an
+    fp16 embedding value is exact in float32 too; `matvec` widens the stored
+    matrix back to float64, so the products are the same.
     """
 
     def __init__(self, cfg: OracleConfig, tensors: Mapping[str, np.ndarray] | Callable[[str], np.ndarray],
-                 cache_dequant: bool = False):
+                 cache_dequant: bool = False, cache_dtype=np.float64):
         self.cfg = cfg
         self._get = tensors if callable(tensors) else tensors.__getitem__
         self._cache: dict[str, np.ndarray] | None = {} if cache_dequant else None
+        self._cache_dtype = np.dtype(cache_dtype)
+        if self._cache_dtype not in (np.dtype(np.float64), np.dtype(np.float32)):
+            raise ValueError("cache_dtype must be float64 or float32")
 
     def _shape(self, name: str) -> tuple[str, int, int]:
         c = self.cfg
@@ -93,6 +101,11 @@ class OracleModel:
         kind, rows, cols = self._shape(name)
         w = dequant(self._get(name), kind, rows, cols)
         if self._cache is not None:
+            if self._cache_dtype != w.dtype:
+                narrow = w.astype(self._cache_dtype)
+                if not np.array_equal(narrow, w):
+                    raise ValueError(f"{name}: dequantised values are not exact in {self._cache_dtype}")
+                w = narrow
             self._cache[name] = w
         return w
 

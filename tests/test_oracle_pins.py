@@ -325,6 +325,29 @@ def check_batch_equals_single(shape=TINY):
         np.testing.assert_allclose(lb[i], ls[0], rtol=1e-13, atol=1e-15)
 
 
+def check_greedy(shape=TINY):
+    """A greedy chain feeds each sequence's own argmax back at the next position.
+
+    Pinned against the uncached recompute (itself pinned by the cached-vs-uncached
+    and torch checks): from an empty cache, the logits of step s of sequence b
+    equal the from-scratch logits of the tokens fed to b so far at positions
+    0..s, and the token fed at step s + 1 is their argmax.  Three sequences with
+    different first tokens, of which only two (out of order) are computed.
+    """
+    model = oracle_model(shape)
+    steps, tokens0, seqs = 4, [5, 9, 11], [2, 0]
+    cache = oracle.OracleCache(oracle_config(shape), 3, steps)
+    fed, logits = oracle.decode.greedy(model, cache, tokens0, [0, 0, 0], steps, seqs=seqs)
+    assert fed.shape == (steps, 2) and logits.shape == (steps, 2, shape.vocab)
+    for i, b in enumerate(seqs):
+        seq = [tokens0[b]]
+        for s in range(steps):
+            assert fed[s, i] == seq[s], (b, s, fed[:, i], seq)
+            want = oracle.uncached_logits(model, seq)
+            np.testing.assert_allclose(logits[s, i], want, rtol=1e-11, atol=1e-13)
+            seq.append(int(np.argmax(want)))
+
+
 def check_argmax():
     lg = np.array([[1.0, 3.0, 3.0, -np.inf], [np.nan, 0.5, 0.5, 0.1], [np.inf, 2.0, np.inf, 1.0]])
     am, nf = oracle.decode._argmax_flag(lg)
@@ -356,6 +379,10 @@ def test_cached_equals_uncached(shape):
 
 def test_batch_equals_single():
     check_batch_equals_single()
+
+
+def test_greedy_chain():
+    check_greedy()
 
 
 # ------------------------------------------------------------------------------------------
@@ -416,6 +443,29 @@ def _matvec_T(w, x):
     return np.asarray(x, np.float64) @ w.T[: w.shape[1], : w.shape[0]].T if w.shape[0] == w.shape[1] else (w.T @ np.asarray(x).T).T
 
 
+def _greedy_variant(stuck_position: bool, wrong_slot: bool):
+    """oracle.greedy with one plausible slip: the position never advances, or the argmax is written to the
+    first len(seqs) sequences instead of the computed ones."""
+    def run(model, cache, tokens, positions, steps, seqs=None):
+        tok = np.array(tokens, dtype=np.int64)
+        pos = np.array(positions, dtype=np.int64)
+        seqs = list(range(len(tok))) if seqs is None else list(seqs)
+        fed, out = [], []
+        for _ in range(steps):
+            fed.append(tok[seqs].copy())
+            logits, am, _ = oracle.decode.decode_step(model, cache, tok, pos, seqs=seqs)
+            out.append(logits)
+            if wrong_slot:
+                tok[:len(seqs)] = am
+            else:
+                tok[seqs] = am
+            if not stuck_position:
+                pos[seqs] += 1
+        return np.array(fed), np.array(out)
+    run.__name__ = "_greedy_stuck_position" if stuck_position else "_greedy_wrong_slot"
+    return run
+
+
 MISTAKES = [
     ("blocks", "dequant_q4_0", _q4_swapped, check_q4_0_hand_blocks),
     ("blocks", "dequant_q8_0", _q8_unsigned, check_q8_0_hand_blocks),
@@ -426,12 +476,14 @@ MISTAKES = [
     ("ops", "rmsnorm", _rms_eps_out, check_rmsnorm),
     ("ops", "silu", _silu_sigmoid, check_silu),
     ("ops", "matvec", _matvec_T, check_matvec),
+    ("decode", "greedy", _greedy_variant(True, False), check_greedy),
+    ("decode", "greedy", _greedy_variant(False, True), check_greedy),
 ]
 
 
 @pytest.mark.parametrize("mod,name,bad,pin", MISTAKES, ids=[m[2].__name__ for m in MISTAKES])
 def test_planted_mistakes(monkeypatch, mod, name, bad, pin):
-    module = {"blocks": oracle.blocks, "ops": oracle.ops}[mod]
+    module = {"blocks": oracle.blocks, "ops": oracle.ops, "decode": oracle.decode}[mod]
     monkeypatch.setitem(module.__dict__, "_orig_" + name, getattr(module, name))
     monkeypatch.setattr(module, name, bad)
     with pytest.raises((AssertionError, ValueError)):
