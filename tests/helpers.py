@@ -91,3 +91,52 @@ def logits_close(got, want, max_abs=2e-3, rel=1e-4):
 def top2_gap(logits):
     s = np.sort(np.asarray(logits, np.float64))
     return float(s[-1] - s[-2])
+
+
+# ------------------------------------------------------------------------------------------
+# derived tolerance of the new layer-0 K/V cache rows
+# ------------------------------------------------------------------------------------------
+U32 = 2.0 ** -24  # unit roundoff of fp32
+
+
+def layer0_kv_tolerance(model, shape, token: int, pos: int):
+    """Element-wise bound on |GPU fp16 row - oracle fp16 row| for the K and V rows that layer 0 appends for
+    `token` at `pos`, derived from the GPU's fp32 arithmetic.
+
+    Layer 0's input x is the embedding row, exact on both sides.  Before the fp16 rounding the GPU's value of
+    element i of y = f * (W (g * x)) (f = 1 / sqrt(mean(x^2) + eps), the RMSNorm factor) differs from the exact
+    one by at most
+      delta_i = f * (blocks + 9) * 2^-23 * sum_k |w_ik g_k x_k|   (the GEMV bound, with one more 2^-24 per
+                                                                  term for the fp32 product g * x)
+              + |y_i| * ((K/64 + 15) * 2^-24 + 2^-23)            (f: a sum of K positive squares at depth at
+                                                                  most K/32 + 24, /K, + eps, sqrt and 1/x each
+                                                                  rounded once; the product f * sum)
+    and a rotated K pair (a, b) by at most delta_a + delta_b + (|y_a| + |y_b|) * 2^-22 (fp32 cos/sin and the
+    rotation's two products and one sum).  Two values within delta round to fp16 values at most
+    delta + one fp16 ulp (at the larger magnitude) apart.  Returns (tol_k, tol_v), each [n_kv_heads * hd].
+    """
+    s = shape
+    x = model.embedding_rows([token])[0]
+    g = model.gain("blk.0.attn_norm.weight")
+    K = s.dim
+    f = 1.0 / np.sqrt(np.mean(x * x) + s.rms_eps)
+    u = x * g
+
+    def pre(name):
+        w = model.matrix(name)
+        y = f * (w.astype(np.float64) @ u)
+        gb = (K // 32 + 9) * 2.0 ** -23 * (np.abs(w.astype(np.float64)) @ np.abs(u))
+        return y, f * gb + np.abs(y) * ((K / 64 + 15) * U32 + 2 * U32)
+
+    yk, dk = pre("blk.0.attn_k.weight")
+    yv, dv = pre("blk.0.attn_v.weight")
+    # rotation: the pair's two errors and the rotation's own rounding
+    dpair = dk[0::2] + dk[1::2] + (np.abs(yk[0::2]) + np.abs(yk[1::2])) * 4 * U32
+    dk_rot = np.repeat(dpair, 2)
+    kr = oracle.rope(yk.reshape(s.n_kv_heads, s.head_dim), pos, s.rope_base).reshape(-1)
+
+    def tol(y, d):
+        big = np.abs(y) + d
+        return np.abs(np.spacing(big.astype(np.float16))).astype(np.float64) + d
+
+    return tol(kr, dk_rot), tol(yv, dv)

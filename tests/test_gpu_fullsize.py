@@ -1,18 +1,15 @@
-"""GPU parity at the benchmark's full sizes (the 7B-shaped Q4_0 and the 8B-shaped
-16-sequence Q8_0 workloads), in the schedule bench.py times.
+"""GPU parity at the benchmark's full sizes: the 7B-shaped Q4_0 workload (64 chained greedy steps) and the
+8B-shaped 16-sequence Q8_0 workload (32 chained steps), in the schedule bench.py times.
 
-A whole float64 step of these models takes the oracle minutes, so the step is
-checked on outputs the oracle computes cheaply, and on properties that hold at
-any size:
+Expected values come from the float64 oracle through tests/golden/make_fullsize.py (stored in
+tests/golden/fullsize_<workload>.npz; the oracle needs minutes per chain, so it is not re-run here).  For the
+stored sequences (sequence 0 of the 7B shape; sequences 0 and 15 of the 8B shape) the test checks:
 
-* the new K/V cache rows of layers 0 and 1 at each sampled sequence's position
-  (layer 1's rows depend on all of layer 0: RMSNorm, the Q/K/V projection,
-  RoPE, attention over the whole context, Wo, the SwiGLU FFN and both
-  residuals), against the oracle run on the model cut to its first two
-  layers with the same tensors;
-* the returned argmax is the first maximum of the returned logits, the logits
-  are finite, no device flag is raised;
-* replaying the step graph gives bit-identical logits.
+* the token fed at every chained step is the oracle's (greedy argmax fed back on the device);
+* logits within max-abs 2e-3 and relative L2 1e-4 at the stored steps (first, middle, last);
+* the K and V rows layer 0 appends at the first step, against the oracle run on the model cut to layer 0,
+  within the bound derived from the GPU's fp32 arithmetic (helpers.layer0_kv_tolerance);
+* no device flag is raised, and replaying the first step's graph gives bit-identical logits.
 """
 
 from __future__ import annotations
@@ -26,13 +23,14 @@ import pytest
 
 import oracle
 import synth
-from helpers import oracle_config
+from helpers import gpu_chain, layer0_kv_tolerance, logits_close, oracle_config, top2_gap
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 torch = pytest.importorskip("torch")
 
-CASES = {"llama2_7b_q4": [0], "llama3_8b_q8_b16": [0, 15]}
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+WORKLOADS = ["llama2_7b_q4", "llama3_8b_q8_b16"]
 
 
 def _setup(wl):
@@ -48,56 +46,57 @@ def _setup(wl):
     return model, state
 
 
-def _row_close(got, want):
-    got = np.asarray(got, np.float64)
-    want = np.asarray(want, np.float64)
-    ulp = np.abs(np.spacing(want.astype(np.float16)).astype(np.float64))
-    tol = ulp + 1e-5 * np.max(np.abs(want))
-    bad = np.abs(got - want) > tol
-    assert not bad.any(), f"{bad.sum()} of {bad.size} elements, worst {np.max(np.abs(got - want) - tol)}"
-
-
-@pytest.mark.parametrize("name", list(CASES))
-def test_full_size_step(name):
-    from block_quantized_token_gb300 import er
-    wl = synth.workload(name).with_(steps=2)
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_full_size_chain(name):
+    path = os.path.join(GOLDEN, f"fullsize_{name}.npz")
+    if not os.path.exists(path):
+        pytest.skip(f"{path} missing: run tests/golden/make_fullsize.py {name}")
+    gold = np.load(path)
+    seqs = [int(b) for b in gold["seqs"]]
+    wl = synth.workload(name)
     s = wl.shape
-    seqs = CASES[name]
     model, state = _setup(wl)
     try:
+        fed, hist = gpu_chain(state, wl, wl.steps)  # production schedule, tokens chained on the device
+        _, code, nonfinite = state.device_error()
+        assert code == 0 and nonfinite == 0
+        # replay of the first step (same inputs, same cache rows rewritten): bit-identical logits
         dev = model.device
         tok = torch.tensor(wl.tokens0(), dtype=torch.int32, device=dev)
         pos = torch.tensor(wl.positions0(), dtype=torch.int32, device=dev)
-        logits = torch.empty((wl.batch, s.vocab), dtype=torch.float32, device=dev)
-        argmax = torch.empty(wl.batch, dtype=torch.int32, device=dev)
-        state.step(tok, pos, logits, argmax)  # the graph bench.py replays
-        torch.cuda.synchronize()
-        _, code, nonfinite = state.device_error()
-        assert code == 0 and nonfinite == 0
-        lg = logits.cpu().numpy()
-        am = argmax.cpu().numpy()
-        assert np.isfinite(lg).all()
-        np.testing.assert_array_equal(am, np.argmax(lg, axis=1))
-        # replay: the new cache rows are rewritten with the same values
-        state.step(tok, pos, logits, argmax)
-        torch.cuda.synchronize()
-        np.testing.assert_array_equal(logits.cpu().numpy(), lg)
-
-        rows = {(b, l): state.read_rows(b, l, int(wl.positions0()[b]), 1) for b in seqs for l in (0, 1)}
+        lg = torch.empty((wl.batch, s.vocab), dtype=torch.float32, device=dev)
+        am = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            state.step(tok, pos, lg, am)
+            torch.cuda.synchronize()
+            assert np.array_equal(lg.cpu().numpy().astype(np.float64), hist[0])
+        rows = {b: state.read_rows(b, 0, int(wl.positions0()[b]), 1) for b in seqs}
+        rows = {b: (k.cpu().numpy().reshape(-1), v.cpu().numpy().reshape(-1)) for b, (k, v) in rows.items()}
     finally:
         state.close()
         model.close()
 
-    # the oracle on the first two layers, with the full model's tensors
-    cut = dataclasses.replace(s, n_layers=2)
-    om = oracle.OracleModel(oracle_config(cut), lambda n: synth.weight_tensor(s, n))
+    for i, b in enumerate(seqs):
+        for st in range(wl.steps):
+            gap = gold["top2"][st - 1, i] if st else float("nan")
+            assert fed[st, b] == gold["fed"][st, i], \
+                f"sequence {b}, step {st}: token {fed[st, b]} vs {gold['fed'][st, i]} (top-2 gap {gap:.3e})"
+        for j, st in enumerate(gold["logit_steps"]):
+            logits_close(hist[st, b], gold["logits"][j, i])
+            assert top2_gap(gold["logits"][j, i]) == pytest.approx(gold["top2"][st, i])
+
+    # layer 0's appended rows against the oracle on the model cut to layer 0 (same tensors)
+    cut = dataclasses.replace(s, n_layers=1)
+    om = oracle.OracleModel(oracle_config(cut), lambda n: synth.weight_tensor(s, n), cache_dequant=True,
+                            cache_dtype=np.float32)
     cache = oracle.OracleCache(oracle_config(cut), wl.batch, wl.capacity)
     for b in seqs:
-        for l in (0, 1):
-            k, v = synth.kv_prefill(wl, b, l)
-            cache.fill(b, l, k, v)
+        k, v = synth.kv_prefill(wl, b, 0)
+        cache.fill(b, 0, k, v)
     oracle.decode_step(om, cache, wl.tokens0(), wl.positions0(), seqs=seqs)
-    for (b, l), (k, v) in rows.items():
+    for b in seqs:
         p = int(wl.positions0()[b])
-        _row_close(k.cpu().numpy().reshape(-1), cache.k[b][l][p].reshape(-1))
-        _row_close(v.cpu().numpy().reshape(-1), cache.v[b][l][p].reshape(-1))
+        tk, tv = layer0_kv_tolerance(om, cut, int(wl.tokens0()[b]), p)
+        for got, want, tol in ((rows[b][0], cache.k[b][0][p], tk), (rows[b][1], cache.v[b][0][p], tv)):
+            d = np.abs(got.astype(np.float64) - want.reshape(-1).astype(np.float64))
+            assert (d <= tol).all(), f"sequence {b}: worst excess {np.max(d - tol):.3e}"

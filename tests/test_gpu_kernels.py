@@ -91,6 +91,56 @@ def test_gemv_parity(w_type, rows, cols, batch):
         er.er_matrix_destroy(m)
 
 
+# fp16 scale bit patterns at the format's edges: 1, -0.5, the largest finite (65504), the smallest normal
+# (2^-14), the smallest subnormal (2^-24), -0, an inexact third, -3 (the same list the oracle's pins use)
+EDGE_SCALES = [0x3C00, 0xB800, 0x7BFF, 0x0400, 0x0001, 0x8000, 0x3555, 0xC200]
+
+
+def _edge_matrix(w_type, rows, cols):
+    """GGUF bytes whose blocks cycle through EDGE_SCALES and, over every 8 consecutive blocks, through every
+    int8 value (Q8_0) or every nibble in both positions of a byte (Q4_0)."""
+    nb = rows * cols // 32
+    bpb = {"q8_0": 34, "q4_0": 18}[w_type]
+    out = np.zeros((nb, bpb), np.uint8)
+    for i in range(nb):
+        out[i, 0:2] = np.frombuffer(np.uint16(EDGE_SCALES[i % len(EDGE_SCALES)]).tobytes(), np.uint8)
+        if w_type == "q8_0":
+            out[i, 2:] = (np.arange(32) + 32 * (i % 8)) % 256  # int8 bytes 0..255 over 8 blocks
+        else:
+            j = np.arange(16)
+            out[i, 2:] = ((j + i) % 16) | (((j + 3 * i + 5) % 16) << 4)
+    return out.reshape(rows, cols // 32 * bpb)
+
+
+@pytest.mark.parametrize("w_type", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("rows,cols", [(48, 256), (40, 544)])
+def test_edge_scales(w_type, rows, cols):
+    """Blocks with subnormal, largest, zero-signed and negative fp16 scales and every quantised value: the
+    dequantisation is bit-exact and the GEMV stays under its bound, on the GPU through the C ABI."""
+    er = _er()
+    raw = _edge_matrix(w_type, rows, cols)
+    dev = torch.from_numpy(raw).cuda()
+    m = er.er_matrix_create(er.DTYPES[w_type], rows, cols, dev.data_ptr())
+    try:
+        out = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+        er.er_matrix_dequant(m, out.data_ptr())
+        w = oracle.dequant(raw, w_type, rows, cols)
+        rng = np.random.default_rng(rows + cols)
+        x = rng.standard_normal((3, cols)).astype(np.float32)
+        xd = torch.from_numpy(x).cuda()
+        y = torch.empty((3, rows), dtype=torch.float32, device="cuda")
+        er.er_matrix_gemv(m, xd.data_ptr(), 3, y.data_ptr())
+        torch.cuda.synchronize()
+        got = out.cpu().numpy().astype(np.float64)
+        np.testing.assert_array_equal(got, w)
+        assert np.array_equal(np.signbit(got), np.signbit(w)), "sign of zero differs"
+        want = oracle.matvec(w, x.astype(np.float64))
+        ratio = np.abs(y.cpu().numpy().astype(np.float64) - want) / gemv_bound(w, x.astype(np.float64))
+        assert ratio.max() <= 1.0, f"worst error {ratio.max():.3f} of the bound"
+    finally:
+        er.er_matrix_destroy(m)
+
+
 def test_matrix_create_rejects_bad_args():
     er = _er()
     dev = torch.zeros(34 * 4, dtype=torch.uint8, device="cuda")
