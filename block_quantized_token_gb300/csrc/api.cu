@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <string>
 
 #include "common.cuh"
@@ -39,18 +40,28 @@ er_status cuda_fail(cudaError_t e, const char *what) {
         if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
     } while (0)
 
+// Test hooks of the allocation-failure paths: the allocation numbered
+// g_alloc_fail_at from the hook's setting on fails as if the device were out
+// of memory (-1: never), and g_live_allocs counts the device allocations the
+// library holds.
+std::atomic<long long> g_alloc_fail_at{-1};
+std::atomic<long long> g_live_allocs{0};
+
 template <class T>
 cudaError_t dalloc(std::vector<void *> &owner, T **p, size_t bytes) {
+    if (g_alloc_fail_at.load() >= 0 && g_alloc_fail_at.fetch_sub(1) == 0) return cudaErrorMemoryAllocation;
     void *q = nullptr;
     cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
     if (e != cudaSuccess) return e;
     owner.push_back(q);
+    ++g_live_allocs;
     *p = reinterpret_cast<T *>(q);
     return cudaSuccess;
 }
 
 void free_all(std::vector<void *> &owner) {
     for (void *p : owner) cudaFree(p);
+    g_live_allocs -= (long long)owner.size();
     owner.clear();
 }
 
@@ -238,6 +249,8 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
     kv->B = batch;
     kv->cap = capacity;
     kv->cap_stream = nullptr;
+    kv->graph_calls = 0;
+    kv->bar_extra = 0;
     const int D = c.dim, qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim, F = c.ffn_dim, hd = c.head_dim;
     const int G = c.n_heads / c.n_kv_heads;
     attention_plan(hd, c.n_kv_heads, batch, capacity, m->num_sms, &kv->S, &kv->CH);
@@ -573,6 +586,7 @@ static cudaError_t enqueue_persistent(er_kv *kv, const int32_t *tokens, const in
     a.done = kv->done;
     a.flags = kv->flags;
     a.bar = kv->step_bar;
+    a.bar_extra = kv->bar_extra;
     cudaError_t e = cudaMemsetAsync(kv->step_bar, 0, sizeof(unsigned), st);
     if (e == cudaSuccess) e = launch_step(c.w_type, a, m->num_sms, st);
     return e;
@@ -608,12 +622,23 @@ er_status er_decode_step(const int32_t *tokens, const int32_t *positions, er_kv 
     er_status s = check_step(tokens, positions, kv);
     if (s != ER_OK) return s;
     cudaGraphExec_t exec = nullptr;
+    const unsigned long long now = ++kv->graph_calls;
     for (auto &g : kv->graphs)
         if (g.tokens == tokens && g.positions == positions && g.logits == logits && g.argmax == argmax) {
             exec = g.exec;
+            g.last_use = now;
             break;
         }
     if (!exec) {
+        if (kv->graphs.size() >= ER_MAX_GRAPHS) {  // drop the least recently launched graph
+            auto lru = std::min_element(kv->graphs.begin(), kv->graphs.end(),
+                                        [](const er_graph_entry &x, const er_graph_entry &y) {
+                                            return x.last_use < y.last_use;
+                                        });
+            // an executable graph still in flight is freed when it completes
+            cudaGraphExecDestroy(lru->exec);
+            kv->graphs.erase(lru);
+        }
         cudaGraph_t graph = nullptr;
         ER_CUDA(cudaStreamBeginCapture(kv->cap_stream, cudaStreamCaptureModeThreadLocal));
         cudaError_t e = enqueue_step(kv, tokens, positions, logits, argmax, kv->cap_stream, true);
@@ -626,7 +651,7 @@ er_status er_decode_step(const int32_t *tokens, const int32_t *positions, er_kv 
         e = cudaGraphInstantiate(&exec, graph, 0);
         cudaGraphDestroy(graph);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
-        kv->graphs.push_back({tokens, positions, logits, argmax, exec});
+        kv->graphs.push_back({tokens, positions, logits, argmax, exec, now});
     }
     ER_CUDA(cudaGraphLaunch(exec, (cudaStream_t)stream));
     return ER_OK;
@@ -695,6 +720,36 @@ int32_t er_kv_launches_per_step(const er_kv *kv) {
     return 1 + c.n_layers * per_layer + groups(m->head);
 }
 
+int32_t er_kv_cached_graphs(const er_kv *kv) { return kv ? (int32_t)kv->graphs.size() : -1; }
+
+er_status er_kv_inject_wait_shortfall(er_kv *kv, int32_t extra) {
+    if (!kv) return fail(ER_EINVAL, "kv is NULL");
+    if (extra < 0 || extra > (1 << 20)) return fail(ER_EINVAL, "extra must be in 0..2^20");
+    if ((unsigned)extra != kv->bar_extra) {
+        ER_CUDA(cudaDeviceSynchronize());
+        for (auto &g : kv->graphs) cudaGraphExecDestroy(g.exec);
+        kv->graphs.clear();
+        kv->bar_extra = (unsigned)extra;
+    }
+    return ER_OK;
+}
+
+er_status er_set_wait_limit_ns(uint64_t ns) {
+    const unsigned long long v = ns ? (unsigned long long)ns : ER_WAIT_NS;
+    cudaError_t (*set[])(unsigned long long) = {set_wait_limit_gemv, set_wait_limit_wide, set_wait_limit_tc,
+                                                set_wait_limit_step_q8, set_wait_limit_step_q4, set_wait_limit_attn};
+    for (auto f : set) ER_CUDA(f(v));
+    return ER_OK;
+}
+
+er_status er_debug_fail_allocation(int64_t n) {
+    if (n < -1) return fail(ER_EINVAL, "n must be >= -1");
+    g_alloc_fail_at.store(n);
+    return ER_OK;
+}
+
+int64_t er_debug_live_allocations(void) { return g_live_allocs.load(); }
+
 er_status er_positions_increment(int32_t *positions, int32_t batch, void *stream) {
     if (!positions || batch < 1) return fail(ER_EINVAL, "bad positions/batch");
     ER_CUDA(launch_positions_increment(positions, batch, (cudaStream_t)stream));
@@ -753,6 +808,7 @@ void er_matrix_destroy(er_matrix *x) {
     cudaFree(x->part);
     cudaFree(x->cnt);
     cudaFree(x->flags);
+    g_live_allocs -= 4;
     delete x;
 }
 

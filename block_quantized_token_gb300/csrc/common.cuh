@@ -15,10 +15,20 @@
 #define ER_FLAG_WAIT 4
 #define ER_FLAG_NONFINITE 8
 
-// bounded waits give up after this many nanoseconds of %globaltimer
+// bounded waits give up after this many nanoseconds of %globaltimer by default
 #define ER_WAIT_NS 1000000000ull
 
 namespace er {
+
+// The limit of every bounded wait, in ns.  Each translation unit holds its own
+// copy (the library is compiled without relocatable device code); the host
+// sets all of them through er_set_wait_limit_ns, for tests of the give-up path.
+static __device__ unsigned long long g_wait_ns = ER_WAIT_NS;
+ER_DEV unsigned long long wait_limit_ns() { return *reinterpret_cast<volatile unsigned long long *>(&g_wait_ns); }
+// Sets this translation unit's copy on the current device (synchronous).
+static inline cudaError_t set_wait_limit_here(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_wait_ns, &ns, sizeof ns);
+}
 
 // ---------------------------------------------------------------------------
 // programmatic dependent launch (PDL)
@@ -83,14 +93,15 @@ ER_DEV uint64_t globaltimer_ns() {
     return t;
 }
 
-// Bounded wait: false after ER_WAIT_NS without completion (the caller records
-// an error and stops waiting).
+// Bounded wait: false after the wait limit without completion (the caller
+// records an error and stops waiting).
 ER_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const unsigned long long lim = wait_limit_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255) == 0 && globaltimer_ns() - t0 > ER_WAIT_NS) return false;
+        if ((i & 255) == 0 && globaltimer_ns() - t0 > lim) return false;
     }
 }
 

@@ -149,6 +149,7 @@ struct StepArgs {
     unsigned long long *amax;
     int *done, *flags;
     unsigned *bar;  // grid barrier counter (zeroed before each launch)
+    unsigned bar_extra;  // arrivals the first barrier waits for beyond the grid (0; > 0 only to test give-up)
 };
 // Whether the persistent step can run this shape (batch, GQA group, head dim,
 // shared memory) and the launch itself (cooperative, one CTA per SM).
@@ -171,6 +172,14 @@ struct EmbedArgs {
 };
 cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_positions_increment(int32_t *pos, int n, cudaStream_t st);
+
+// every translation unit's copy of the bounded-wait limit (common.cuh), on the current device
+cudaError_t set_wait_limit_gemv(unsigned long long ns);
+cudaError_t set_wait_limit_wide(unsigned long long ns);
+cudaError_t set_wait_limit_tc(unsigned long long ns);
+cudaError_t set_wait_limit_step_q8(unsigned long long ns);
+cudaError_t set_wait_limit_step_q4(unsigned long long ns);
+cudaError_t set_wait_limit_attn(unsigned long long ns);
 
 }  // namespace er
 
@@ -207,9 +216,13 @@ struct er_model {
     std::vector<void *> allocs;
 };
 
+// recorded step graphs an er_kv keeps (one per pointer set; least recently used dropped first)
+#define ER_MAX_GRAPHS 8
+
 struct er_graph_entry {
     const void *tokens, *positions, *logits, *argmax;
     cudaGraphExec_t exec;
+    unsigned long long last_use;  // er_decode_step call count at its last launch
 };
 
 struct er_kv {
@@ -234,6 +247,8 @@ struct er_kv {
     int *done;
     int *flags;
     cudaStream_t cap_stream;
-    std::vector<er_graph_entry> graphs;
+    std::vector<er_graph_entry> graphs;  // at most ER_MAX_GRAPHS, least recently used dropped first
+    unsigned long long graph_calls;
+    unsigned bar_extra;                  // injected barrier shortfall (tests of the give-up path)
     std::vector<void *> allocs;
 };

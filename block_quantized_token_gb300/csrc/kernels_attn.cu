@@ -421,4 +421,7 @@ cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl) {
     return cudaErrorInvalidValue;
 }
 
+// this translation unit's copy of the bounded-wait limit
+cudaError_t set_wait_limit_attn(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 }  // namespace er

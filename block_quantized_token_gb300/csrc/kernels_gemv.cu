@@ -165,6 +165,9 @@ cudaError_t launch_gemv(int epi, const GemvArgs &a, int num_sms, cudaStream_t st
     return cudaErrorInvalidValue;
 }
 
+// this translation unit's copy of the bounded-wait limit
+cudaError_t set_wait_limit_gemv(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 }  // namespace er
 
 // ---------------------------------------------------------------------------
@@ -213,8 +216,11 @@ extern "C" er_status er_matrix_gemv_noalloc(const er_matrix *x, const float *xin
     if (x->num_sms > NOALLOC_MAX_SMS) return er_fail_status(ER_EUNSUPPORTED, "more SMs than the fixed scratch holds");
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return er_fail_cuda(e, "er_matrix_gemv_noalloc set-up");
+    // the array used is the current device's; the matrix (and its SM count) must belong to that device
+    if (device != x->device) return er_fail_status(ER_EINVAL, "the matrix belongs to another device than the current one");
     unsigned char *base = nullptr;
-    if (e == cudaSuccess) e = noalloc_scratch_for(device, &base);
+    e = noalloc_scratch_for(device, &base);
     if (e != cudaSuccess) return er_fail_cuda(e, "er_matrix_gemv_noalloc set-up");
     cudaStream_t st = (cudaStream_t)stream;
     GemvArgs a = {};
@@ -240,4 +246,21 @@ extern "C" er_status er_matrix_gemv_noalloc(const er_matrix *x, const float *xin
     }
     if (e != cudaSuccess) return er_fail_cuda(e, "er_matrix_gemv_noalloc");
     return ER_OK;
+}
+
+extern "C" er_status er_matrix_gemv_noalloc_error(int32_t *code) {
+    using namespace er;
+    if (!code) return er_fail_status(ER_EINVAL, "NULL argument");
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    unsigned char *base = nullptr;
+    if (e == cudaSuccess) e = noalloc_scratch_for(device, &base);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int *flag = reinterpret_cast<int *>(base + NOALLOC_PART_BYTES + NOALLOC_CNT_BYTES);
+    int f = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&f, flag, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(flag, 0, sizeof(int));
+    if (e != cudaSuccess) return er_fail_cuda(e, "er_matrix_gemv_noalloc_error");
+    *code = f & ER_FLAG_WAIT;
+    return *code ? er_fail_status(ER_EDEVICE, "a wait in er_matrix_gemv_noalloc gave up") : ER_OK;
 }

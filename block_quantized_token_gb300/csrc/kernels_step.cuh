@@ -21,8 +21,9 @@
 //   GATEUP  a = silu(Wgate h2) * (Wup h2), h2 = RMSNorm(x)
 //   DOWN    x += Wdown a
 //   HEAD    logits = Wout RMSNorm(x); argmax
-// Every barrier wait is bounded (about a second of %globaltimer); a wait that
-// gives up sets a device flag and every CTA returns after draining its copies.
+// Every barrier wait is bounded (a second of %globaltimer by default); a wait
+// that gives up sets a device flag and every CTA returns after draining its
+// copies.
 #pragma once
 
 #include "gemv_core.cuh"
@@ -43,16 +44,18 @@ __host__ __device__ inline size_t mk_smem_bytes(int max_k, int B, int hd, int G)
 }
 
 // Grid barrier number `gen` (1, 2, ...): every CTA adds 1 to *bar, then waits
-// until *bar reaches gen * gridDim.x.  Returns false (all threads) if the wait
-// gave up or another CTA flagged an error.
-__device__ inline bool mk_barrier(unsigned *bar, int *flags, unsigned gen, int *ok_smem) {
+// until *bar reaches gen * gridDim.x + extra (extra > 0 only when a test
+// injects a shortfall: then no CTA can pass and every wait gives up).  Returns
+// false (all threads) if the wait gave up or another CTA flagged an error.
+__device__ inline bool mk_barrier(unsigned *bar, int *flags, unsigned gen, int *ok_smem, unsigned extra = 0) {
     __syncthreads();
     if (threadIdx.x == 0) {
         red_add_release_gpu(bar, 1);
-        const unsigned target = gen * gridDim.x;
+        const unsigned target = gen * gridDim.x + extra;
         bool ok = true;
         if (ld_acquire_gpu(bar) < target) {
             const uint64_t t0 = globaltimer_ns();
+            const unsigned long long lim = wait_limit_ns();
             for (uint32_t i = 1;; ++i) {
                 if (ld_acquire_gpu(bar) >= target) break;
                 if ((i & 31) == 0) {
@@ -60,7 +63,7 @@ __device__ inline bool mk_barrier(unsigned *bar, int *flags, unsigned gen, int *
                         ok = false;
                         break;
                     }
-                    if (globaltimer_ns() - t0 > ER_WAIT_NS) {
+                    if (globaltimer_ns() - t0 > lim) {
                         atomicOr(flags, ER_FLAG_WAIT);
                         ok = false;
                         break;
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(GV_WARPS * 32, 1) step_kernel(const StepArgs p
                                : repacked_value(p.head, QT, p.UPR[4], tok, k);
             p.x[(size_t)b * p.D + k] = v;
         }
-        ok = mk_barrier(p.bar, p.flags, ++gen, &ok_smem);
+        ok = mk_barrier(p.bar, p.flags, ++gen, &ok_smem, p.bar_extra);
     }
 
     // one GEMV phase; every thread of the CTA takes the same path through the

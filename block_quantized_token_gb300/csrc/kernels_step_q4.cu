@@ -68,4 +68,7 @@ cudaError_t launch_step_q4(const StepArgs &a, int num_sms, size_t smem, cudaStre
     return cudaErrorInvalidValue;
 }
 
+// this translation unit's copy of the bounded-wait limit
+cudaError_t set_wait_limit_step_q4(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 }  // namespace er

@@ -114,4 +114,7 @@ cudaError_t launch_step(int qt, const StepArgs &a, int num_sms, cudaStream_t st)
     return qt == Q8_0 ? launch_step_q8(a, num_sms, smem, st) : launch_step_q4(a, num_sms, smem, st);
 }
 
+// this translation unit's copy of the bounded-wait limit
+cudaError_t set_wait_limit_step_q8(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 }  // namespace er

@@ -477,4 +477,7 @@ cudaError_t launch_gemv_wide(int epi, const GemvArgs &a, float *wpart, float *ws
     return cudaErrorInvalidValue;
 }
 
+// this translation unit's copy of the bounded-wait limit
+cudaError_t set_wait_limit_wide(unsigned long long ns) { return set_wait_limit_here(ns); }
+
 }  // namespace er

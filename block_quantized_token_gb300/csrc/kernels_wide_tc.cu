@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) gemv_tc_kernel(const GemvArgs a
             const unsigned need = 4u * (unsigned)(tile + 1);
             const uint64_t t0 = globaltimer_ns();
             while (ld_acquire_cta(tiles_done + w) < need) {
-                if (*abort_s || globaltimer_ns() - t0 > ER_WAIT_NS) {
+                if (*abort_s || globaltimer_ns() - t0 > wait_limit_ns()) {
                     bad = true;
                     break;
                 }
@@ -777,5 +777,8 @@ cudaError_t launch_gemv_tc(int epi, const GemvArgs &a, float *wpart, float *wssq
     }
     return cudaErrorInvalidValue;
 }
+
+// this translation unit's copy of the bounded-wait limit
+cudaError_t set_wait_limit_tc(unsigned long long ns) { return set_wait_limit_here(ns); }
 
 }  // namespace er

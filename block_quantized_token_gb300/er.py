@@ -75,6 +75,12 @@ def _load() -> ctypes.CDLL:
         "er_matrix_dequant": (I32, [VP, VP, VP]),
         "er_matrix_gemv": (I32, [VP, VP, I32, VP, VP]),
         "er_matrix_gemv_noalloc": (I32, [VP, VP, I32, VP, VP]),
+        "er_matrix_gemv_noalloc_error": (I32, [P(I32)]),
+        "er_kv_cached_graphs": (I32, [VP]),
+        "er_kv_inject_wait_shortfall": (I32, [VP, I32]),
+        "er_set_wait_limit_ns": (I32, [ctypes.c_uint64]),
+        "er_debug_fail_allocation": (I32, [ctypes.c_int64]),
+        "er_debug_live_allocations": (ctypes.c_int64, []),
         "er_status_str": (ctypes.c_char_p, [I32]),
         "er_last_error": (ctypes.c_char_p, []),
     }
@@ -90,7 +96,9 @@ EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_
             "er_kv_layer_ptrs", "er_kv_write", "er_kv_read", "er_decode_step", "er_decode_step_eager", "er_positions_increment",
             "er_kv_set_schedule", "er_kv_get_schedule", "er_kv_set_wide_gemv",
             "er_get_device_error", "er_launch_stage", "er_matrix_create", "er_matrix_destroy",
-            "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_kv_launches_per_step", "er_status_str", "er_last_error")
+            "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_matrix_gemv_noalloc_error",
+            "er_kv_launches_per_step", "er_kv_cached_graphs", "er_kv_inject_wait_shortfall", "er_set_wait_limit_ns",
+            "er_debug_fail_allocation", "er_debug_live_allocations", "er_status_str", "er_last_error")
 
 
 def lib() -> ctypes.CDLL:
@@ -215,3 +223,32 @@ def er_matrix_gemv(mat: int, x: int, batch: int, y: int, stream: int = 0) -> Non
 
 def er_matrix_gemv_noalloc(mat: int, x: int, batch: int, y: int, stream: int = 0) -> None:
     _check(_lib.er_matrix_gemv_noalloc(mat, x, batch, y, stream), "er_matrix_gemv_noalloc")
+
+
+def er_matrix_gemv_noalloc_error() -> tuple[int, int]:
+    """Returns (status, code) without raising on ER_EDEVICE."""
+    code = ctypes.c_int32()
+    st = _lib.er_matrix_gemv_noalloc_error(ctypes.byref(code))
+    if st not in (ER_OK, ER_EDEVICE):
+        _check(st, "er_matrix_gemv_noalloc_error")
+    return st, code.value
+
+
+def er_kv_cached_graphs(kv: int) -> int:
+    return int(_lib.er_kv_cached_graphs(kv))
+
+
+def er_kv_inject_wait_shortfall(kv: int, extra: int) -> None:
+    _check(_lib.er_kv_inject_wait_shortfall(kv, extra), "er_kv_inject_wait_shortfall")
+
+
+def er_set_wait_limit_ns(ns: int) -> None:
+    _check(_lib.er_set_wait_limit_ns(ns), "er_set_wait_limit_ns")
+
+
+def er_debug_fail_allocation(n: int) -> None:
+    _check(_lib.er_debug_fail_allocation(n), "er_debug_fail_allocation")
+
+
+def er_debug_live_allocations() -> int:
+    return int(_lib.er_debug_live_allocations())

@@ -195,6 +195,36 @@ ER_API er_status er_positions_increment(int32_t *positions_dev, int32_t batch, v
  * Returns ER_EDEVICE if *code != 0, else ER_OK. */
 ER_API er_status er_get_device_error(er_kv *kv, int32_t *code, int32_t *non_finite);
 
+/* Recorded step graphs kv holds (one per set of pointers passed to
+ * er_decode_step), or -1 for NULL.  At most 8 are kept: a call with a new
+ * pointer set beyond that drops the least recently launched graph (a dropped
+ * graph still running finishes normally), so a caller that rotates buffers
+ * holds a bounded number of graphs. */
+ER_API int32_t er_kv_cached_graphs(const er_kv *kv);
+
+/* Failure injection for tests of the bounded waits, on the host side; it
+ * mirrors the pages' check of a command buffer's status and timeout ("llama.cpp
+ * Metal (MPS) End-to-End Inference Path", step table).  With extra > 0 the
+ * first grid barrier of the persistent step waits for `extra` more arrivals
+ * than its grid can supply, so every CTA's wait runs out: the kernel returns,
+ * er_get_device_error reports bit 2, and that step's outputs are unspecified.
+ * extra = 0 (the default) restores normal steps.  Drops kv's recorded graphs;
+ * has no effect under ER_SCHEDULE_KERNELS.  ER_EINVAL outside 0..2^20. */
+ER_API er_status er_kv_inject_wait_shortfall(er_kv *kv, int32_t extra);
+/* Limit of every bounded wait in the library's kernels (grid barriers, ring
+ * and pipeline waits), in nanoseconds of %globaltimer, on the current device;
+ * 0 restores the default of one second.  Synchronous.  For tests that make a
+ * wait run out in milliseconds. */
+ER_API er_status er_set_wait_limit_ns(uint64_t ns);
+/* Test hooks of the allocation-failure paths.  After er_debug_fail_allocation(n)
+ * the library's device allocation number n from now on (0 = the next one)
+ * fails as if the device were out of memory, so the call making it returns
+ * ER_ENOMEM and frees what it had taken; n = -1 (the default) turns the hook
+ * off.  er_debug_live_allocations gives the number of device allocations the
+ * library currently holds (models, decode states, matrices). */
+ER_API er_status er_debug_fail_allocation(int64_t n);
+ER_API int64_t er_debug_live_allocations(void);
+
 /* Stage kernels of the per-phase schedule (ER_SCHEDULE_KERNELS), queued alone
  * with the step's own arguments for layer `layer` (ignored by EMBED and HEAD).
  * For per-kernel timing. */
@@ -240,10 +270,20 @@ ER_API er_status er_matrix_gemv(const er_matrix *mat, const float *x_dev, int32_
  *     call clears the part that must start at zero.  Calls that overlap on the
  *     GPU (other streams, other threads) race on it: serialise them.
  *   - Limits: at most 262144 rows (16384 row groups) and 256 SMs; larger
- *     matrices give ER_EINVAL, more SMs ER_EUNSUPPORTED.
+ *     matrices give ER_EINVAL, more SMs ER_EUNSUPPORTED.  `mat` must belong to
+ *     the current device (else ER_EINVAL).
+ *   - A bounded wait that gives up inside a call is not returned by the call
+ *     (it is queued asynchronously): er_matrix_gemv_noalloc_error reports it.
  * There is no counterpart on the pages; it exists for this library's callers. */
 ER_API er_status er_matrix_gemv_noalloc(const er_matrix *mat, const float *x_dev, int32_t batch, float *y_dev,
                                         void *stream);
+/* Synchronises the current device, then reports and clears the flag word of
+ * er_matrix_gemv_noalloc's array there: *code = 4 if a bounded wait inside the
+ * most recent call on this device gave up (its y_dev is then unspecified),
+ * else 0.  Every call clears the flag when it starts, so query after each call
+ * whose result matters.  Returns ER_EDEVICE if *code != 0.  Allocates nothing.
+ * No counterpart on the pages. */
+ER_API er_status er_matrix_gemv_noalloc_error(int32_t *code);
 
 ER_API const char *er_status_str(er_status s);
 ER_API const char *er_last_error(void);
