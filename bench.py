@@ -33,6 +33,8 @@ import synth  # noqa: E402
 
 METRIC = "decode tok/s per step and achieved HBM GB/s vs 8 TB/s roofline (Q8_0/Q4_0)"
 BPB = {"q8_0": 34, "q4_0": 18}
+NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s roofline the metric names
+DEFAULT_WORKLOAD = "llama3_8b_q8_b16"  # the largest single-GPU workload, one of the two the 70 % target names
 
 
 # ----------------------------------------------------------------------------------------------
@@ -79,18 +81,22 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-# DRAM bytes per launch of the step kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by workload and by a hash of the kernel's sources at the capture:
-# a changed kernel reports no traffic until it is captured again.
-KERNEL_TRAFFIC = {
-    # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --steps 4 --warmup 3 --no-cpu-baseline`
-    "smollm_q8": ("35d7ab1969b026e2", 190641152 + 3227648),
+# sources each measured kernel is compiled from
+KERNEL_SOURCES = {
+    "step_kernel": ("common.cuh", "gemv_core.cuh", "internal.h", "kernels_step.cuh", "kernels_step_q4.cu",
+                    "kernels_step_q8.cu", "layout.cuh"),
+    "attn": ("common.cuh", "internal.h", "kernels_attn.cu"),
 }
+STEP_KERNEL_SOURCES = KERNEL_SOURCES["step_kernel"]
 
-
-# sources the persistent step kernel is compiled from
-STEP_KERNEL_SOURCES = ("common.cuh", "gemv_core.cuh", "internal.h", "kernels_step.cuh", "kernels_step_q4.cu",
-                       "kernels_step_q8.cu", "layout.cuh")
+# DRAM bytes per launch of a kernel from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum),
+# keyed by (workload, kernel) with a hash of that kernel's sources at the capture: a changed kernel
+# reports no traffic until it is captured again.  Captures of a cut model (fewer layers) are per launch
+# of the same kernel on the same per-layer shapes.
+KERNEL_TRAFFIC = {
+    # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --workload smollm_q8 --steps 4 --warmup 3 --no-cpu-baseline`
+    ("smollm_q8", "step_kernel"): ("35d7ab1969b026e2", 190641152 + 3227648),
+}
 
 
 def csrc_hash(files=STEP_KERNEL_SOURCES) -> str:
@@ -109,9 +115,9 @@ def csrc_hash(files=STEP_KERNEL_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def kernel_traffic(workload: str):
-    e = KERNEL_TRAFFIC.get(workload)
-    return e[1] if e and e[0] == csrc_hash() else None
+def kernel_traffic(workload: str, kernel: str = "step_kernel"):
+    e = KERNEL_TRAFFIC.get((workload, kernel))
+    return e[1] if e and e[0] == csrc_hash(KERNEL_SOURCES[kernel]) else None
 
 
 def max_over_ranks(value: float, device) -> float:
@@ -246,17 +252,22 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     # kernel's own duration; the outer pair times the whole chain
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
     torch.cuda.synchronize(dev)
-    ev0.record(stream)
-    for i in range(K):
-        evs[i][0].record(stream)
-        er.er_decode_step(tok.data_ptr(), pos.data_ptr(), state.handle, logits.data_ptr(), tok.data_ptr(), sp)
-        evs[i][1].record(stream)
-        er.er_positions_increment(pos.data_ptr(), B, sp)
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(K):
+            if flush is not None:  # a write larger than L2 between steps (outside the per-step events)
+                flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            er.er_decode_step(tok.data_ptr(), pos.data_ptr(), state.handle, logits.data_ptr(), tok.data_ptr(), sp)
+            evs[i][1].record(stream)
+            er.er_positions_increment(pos.data_ptr(), B, sp)
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = ev0.elapsed_time(ev1)
     graph_ms = [a.elapsed_time(b) for a, b in evs]
+    # with the flush, the step time is the sum of the step graphs alone
+    ms = sum(graph_ms) if flush is not None else ev0.elapsed_time(ev1)
     clock_info = clocks.stop() if rank == 0 else None
     ms = max_over_ranks(ms, dev)
     st, code, nf = state.device_error()
@@ -303,7 +314,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             launch_ms = float(np.mean(graph_ms))
             achieved = bytes_step / (launch_ms / 1e3) / 1e9
             roof = {"bound": "hbm", "kernel": "step_kernel", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": kernel_traffic(wl.name),
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                    "traffic": kernel_traffic(wl.name),
                     "peak_source": f"{peaks['source']} hbm_gbs (STREAM-style copy)",
                     "bytes_per_launch": bytes_step, "us_per_launch": launch_ms * 1e3,
                     "timing": "CUDA events around each step graph inside the timed region"}
@@ -332,7 +344,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                        "batch": B, "context": wl.prefill, "chained_steps": K, "schedule": schedule,
                        "step_bytes": bytes_step, "step_gbs": bytes_step / (ms / K / 1e3) / 1e9,
                        "step_roofline_frac": bytes_step / (ms / K / 1e3) / 1e9 / measured_peaks()["hbm_gbs"],
-                       "l2": ("inputs larger than L2" if bytes_step > 129e6 else "L2-resident working set"),
+                       "step_frac_of_8tbs": bytes_step / (ms / K / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                       "l2": ("L2 flushed between steps (256 MiB write), step graphs timed alone" if args.flush_l2
+                              else "inputs larger than L2" if bytes_step > 129e6
+                              else "L2-resident working set, not flushed"),
                        "parallelism": f"replicas x{world}", "setup_s": round(setup_s, 1)},
             "e2e": {"value": tokens / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": 8 * B, "d2h_bytes_per_step": 4 * B},
             "gpu_launches": (launches_step + 1) * K,
@@ -382,7 +397,8 @@ def stage_roofline(er, state, wl, tok, pos, logits, stream, dev, iters: int = 20
     top = max(share, key=share.get)
     achieved = sb[top] / (durs[top] / 1e3) / 1e9
     return {"bound": "hbm", "kernel": top, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "frac": achieved / peaks["hbm_gbs"], "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+            "traffic": kernel_traffic(wl.name, top) if top in KERNEL_SOURCES else None,
             "peak_source": f"{peaks['source']} hbm_gbs (burst, kernel timed alone)",
             "bytes_per_launch": sb[top], "us_per_launch": durs[top] * 1e3,
             "stages_us": {n: round(d * 1e3, 2) for n, d in durs.items()},
@@ -486,9 +502,11 @@ def gemv_sweep(reps: int = 50) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=None, help="timed chained steps (default: the workload's chain)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="smollm_q8", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="write 256 MiB between steps and time the step graphs alone (for L2-sized workloads)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--gemv-sweep", action="store_true",
                     help="time the isolated Q4_0 GEMV sweep (576x576, 1536x576, 49152x576) and print it")
@@ -509,6 +527,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     wl = synth.workload(args.workload)
+    if args.steps is None:
+        args.steps = wl.steps
     if args.layers:
         import dataclasses
         wl = wl.with_(name=f"{wl.name}_L{args.layers}", shape=dataclasses.replace(wl.shape, n_layers=args.layers))
