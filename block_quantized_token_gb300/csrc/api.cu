@@ -91,6 +91,17 @@ int device_sms(int *dev) {
 
 }  // namespace
 
+cudaError_t er::device_alloc(void **p, size_t bytes) {
+    std::vector<void *> own;
+    return dalloc(own, p, bytes);
+}
+
+void er::device_free(void *p) {
+    if (!p) return;
+    cudaFree(p);
+    --g_live_allocs;
+}
+
 // error reporting for entry points defined in other files
 er_status er_fail_status(er_status s, const char *msg) { return fail(s, "%s", msg); }
 er_status er_fail_cuda(cudaError_t e, const char *what) { return cuda_fail(e, what); }
@@ -301,6 +312,9 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
             A(&kv->wide_ssq, ssq * sizeof(float), false);
         }
     }
+    if (e == cudaSuccess)
+        e = attention_tensor_maps(kv->kc, kv->vc, (size_t)batch * c.n_layers * c.n_kv_heads * (size_t)capacity, hd,
+                                  &kv->attn_tmk, &kv->attn_tmv);
     A(&kv->amax, 16 * sizeof(unsigned long long));
     A(&kv->done, sizeof(int));
     A(&kv->flags, sizeof(int));
@@ -490,6 +504,8 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
         }
         case ER_STAGE_ATTN: {
             AttnArgs a = {};
+            a.tmk = kv->attn_tmk;
+            a.tmv = kv->attn_tmv;
             a.q = kv->q;
             a.kc = kv->kc;
             a.vc = kv->vc;

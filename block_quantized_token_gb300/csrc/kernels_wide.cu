@@ -25,15 +25,17 @@
 namespace er {
 
 constexpr int GW_WARPS = 16;
+constexpr int GW_SLOTS = 3;                   // ring slots per warp
 constexpr int GW_SLICE_UNITS = 16;            // 1024 columns
 constexpr int GW_NT = 4;                      // n8 tiles: 16 batch columns x (hi, lo)
 constexpr int GW_BLOCK_BYTES = GW_NT * 8 * 64;  // operand bytes of one 32-element block
-constexpr int GW_OFF_RING = 512;
+constexpr int GW_OFF_RING = 1024;             // after the mbarriers (room for 8 slots per warp)
+static_assert(GW_WARPS * GW_SLOTS * 8 <= GW_OFF_RING, "mbarriers overlap the ring");
 
 __host__ __device__ inline int gw_slices(int UPR) { return (UPR + GW_SLICE_UNITS - 1) / GW_SLICE_UNITS; }
 
 template <int QT>
-constexpr int gw_off_operand() { return GW_OFF_RING + GvCfg<QT>::RING; }
+constexpr int gw_off_operand() { return GW_OFF_RING + GW_WARPS * GW_SLOTS * GvCfg<QT>::SLOT; }
 template <int QT>
 constexpr int gw_smem() {
     // operand of 32 blocks, then per-column factors [16], column maxima [16] (uint), per-item sums of squares [512]
@@ -157,15 +159,15 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
     const int my_items = nrg > warp ? (nrg - warp + GW_WARPS - 1) / GW_WARPS : 0;  // rows groups rg0 + warp + 16 i
     const int spi = (nu + C::SU - 1) / C::SU;                                          // ring slots per row group
 
-    uint64_t *wbar = bars + warp * GV_SLOTS;
-    uint8_t *ring = smem + GW_OFF_RING + warp * GV_SLOTS * C::SLOT;
+    uint64_t *wbar = bars + warp * GW_SLOTS;
+    uint8_t *ring = smem + GW_OFF_RING + warp * GW_SLOTS * C::SLOT;
     int p_item = 0, p_slot = 0, issued = 0;
     auto issue_next = [&]() {  // lane 0
         if (p_item >= my_items) return;
         const int rg = rg0 + warp + GW_WARPS * p_item;
         const int u0 = p_slot * C::SU, cnt = min(C::SU, nu - u0);
         const uint32_t bytes = (uint32_t)cnt * C::UB;
-        const unsigned sidx = (unsigned)issued % GV_SLOTS;
+        const unsigned sidx = (unsigned)issued % GW_SLOTS;
         mbar_arrive_expect_tx(wbar + sidx, bytes);
         bulk_g2s(ring + sidx * C::SLOT, a.W + ((size_t)rg * a.UPR + ku0 + u0) * C::UB, bytes, wbar + sidx);
         ++issued;
@@ -175,9 +177,9 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
         }
     };
     if (lane == 0) {
-        for (int i = 0; i < GV_SLOTS; ++i) mbar_init(wbar + i, 1);
+        for (int i = 0; i < GW_SLOTS; ++i) mbar_init(wbar + i, 1);
         fence_mbar_init();
-        for (int i = 0; i < GV_SLOTS; ++i) issue_next();
+        for (int i = 0; i < GW_SLOTS; ++i) issue_next();
     }
     __syncwarp();
 
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
     __syncthreads();
     if (stop_s) {  // an earlier kernel gave up on a wait: drain and stop
         if (lane == 0)
-            for (int k = 0; k < issued; ++k) mbar_wait(wbar + k % GV_SLOTS, (k / GV_SLOTS) & 1);
+            for (int k = 0; k < issued; ++k) mbar_wait(wbar + k % GW_SLOTS, (k / GW_SLOTS) & 1);
         return;
     }
     pdl_launch_dependents();
@@ -299,8 +301,8 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
 #pragma unroll
         for (int jj = 0; jj < GW_NT; ++jj) acc[jj][0] = acc[jj][1] = 0.f;
         for (int sl = 0; sl < spi; ++sl, ++k) {
-            const unsigned sidx = (unsigned)k % GV_SLOTS;
-            if (!mbar_wait(wbar + sidx, ((unsigned)k / GV_SLOTS) & 1u)) {
+            const unsigned sidx = (unsigned)k % GW_SLOTS;
+            if (!mbar_wait(wbar + sidx, ((unsigned)k / GW_SLOTS) & 1u)) {
                 if (lane == 0) atomicOr(a.flags, ER_FLAG_WAIT);
                 failed = true;
                 break;
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
         }
     }
     if (failed && lane == 0)
-        for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % GV_SLOTS, (kk / GV_SLOTS) & 1);
+        for (int kk = k; kk < issued; ++kk) mbar_wait(wbar + kk % GW_SLOTS, (kk / GW_SLOTS) & 1);
 }
 
 // ---------------------------------------------------------------------------

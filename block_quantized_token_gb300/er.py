@@ -81,6 +81,14 @@ def _load() -> ctypes.CDLL:
         "er_set_wait_limit_ns": (I32, [ctypes.c_uint64]),
         "er_debug_fail_allocation": (I32, [ctypes.c_int64]),
         "er_debug_live_allocations": (ctypes.c_int64, []),
+        "er_gguf_open": (I32, [ctypes.c_char_p, P(VP)]),
+        "er_gguf_close": (None, [VP]),
+        "er_gguf_tensor_count": (ctypes.c_int64, [VP]),
+        "er_gguf_tensor_info": (I32, [VP, ctypes.c_int64, P(ctypes.c_char_p), P(I32), P(I32),
+                                      P(ctypes.c_int64), P(VP), P(ctypes.c_uint64)]),
+        "er_gguf_find": (I32, [VP, ctypes.c_char_p, P(ctypes.c_int64)]),
+        "er_gguf_config": (I32, [VP, I32, P(er_config)]),
+        "er_model_create_from_gguf": (I32, [VP, I32, VP, P(VP)]),
         "er_status_str": (ctypes.c_char_p, [I32]),
         "er_last_error": (ctypes.c_char_p, []),
     }
@@ -98,7 +106,9 @@ EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_
             "er_get_device_error", "er_launch_stage", "er_matrix_create", "er_matrix_destroy",
             "er_matrix_dequant", "er_matrix_gemv", "er_matrix_gemv_noalloc", "er_matrix_gemv_noalloc_error",
             "er_kv_launches_per_step", "er_kv_cached_graphs", "er_kv_inject_wait_shortfall", "er_set_wait_limit_ns",
-            "er_debug_fail_allocation", "er_debug_live_allocations", "er_status_str", "er_last_error")
+            "er_debug_fail_allocation", "er_debug_live_allocations", "er_gguf_open", "er_gguf_close",
+            "er_gguf_tensor_count", "er_gguf_tensor_info", "er_gguf_find", "er_gguf_config",
+            "er_model_create_from_gguf", "er_status_str", "er_last_error")
 
 
 def lib() -> ctypes.CDLL:
@@ -115,7 +125,7 @@ def er_status_str(status: int) -> str:
 
 
 def er_last_error() -> str:
-    return _lib.er_last_error().decode()
+    return _lib.er_last_error().decode(errors="replace")
 
 
 def er_model_create(cfg: er_config, weights: er_weights, stream: int = 0) -> int:
@@ -252,3 +262,45 @@ def er_debug_fail_allocation(n: int) -> None:
 
 def er_debug_live_allocations() -> int:
     return int(_lib.er_debug_live_allocations())
+
+
+def er_gguf_open(path: str) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.er_gguf_open(os.fsencode(path), ctypes.byref(out)), "er_gguf_open")
+    return out.value
+
+
+def er_gguf_close(g: int) -> None:
+    _lib.er_gguf_close(g)
+
+
+def er_gguf_tensor_count(g: int) -> int:
+    return int(_lib.er_gguf_tensor_count(g))
+
+
+def er_gguf_tensor_info(g: int, i: int) -> tuple[str, int, list[int], int, int]:
+    """(name, type, dims (innermost first, n_dims of them), host address of the data, bytes)."""
+    name, typ, nd = ctypes.c_char_p(), ctypes.c_int32(), ctypes.c_int32()
+    dims = (ctypes.c_int64 * 4)()
+    data, nbytes = ctypes.c_void_p(), ctypes.c_uint64()
+    _check(_lib.er_gguf_tensor_info(g, i, ctypes.byref(name), ctypes.byref(typ), ctypes.byref(nd), dims,
+                                    ctypes.byref(data), ctypes.byref(nbytes)), "er_gguf_tensor_info")
+    return name.value.decode(errors="replace"), typ.value, list(dims[:nd.value]), data.value or 0, nbytes.value
+
+
+def er_gguf_find(g: int, name: str) -> int:
+    idx = ctypes.c_int64()
+    _check(_lib.er_gguf_find(g, name.encode(), ctypes.byref(idx)), "er_gguf_find")
+    return idx.value
+
+
+def er_gguf_config(g: int, max_batch: int = 1) -> er_config:
+    cfg = er_config()
+    _check(_lib.er_gguf_config(g, max_batch, ctypes.byref(cfg)), "er_gguf_config")
+    return cfg
+
+
+def er_model_create_from_gguf(g: int, max_batch: int = 1, stream: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.er_model_create_from_gguf(g, max_batch, stream, ctypes.byref(out)), "er_model_create_from_gguf")
+    return out.value

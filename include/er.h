@@ -285,6 +285,44 @@ ER_API er_status er_matrix_gemv_noalloc(const er_matrix *mat, const float *x_dev
  * No counterpart on the pages. */
 ER_API er_status er_matrix_gemv_noalloc_error(int32_t *code);
 
+/* GGUF container ("EdgeRunner Core Architecture" section 2.2, Model Loading:
+ * the loader maps the file and parses the model configuration from its
+ * metadata; "alpaca.swift" Capabilities: GGUF v2/v3, F16/Q8_0/Q4_0 tensors).
+ * The file is treated as untrusted: every count, length, dimension and offset
+ * is checked against the bytes present (overflow-checked) before use, and a
+ * malformed file gives ER_EINVAL with the reason in er_last_error().
+ *
+ * er_gguf_open maps `path` read-only (host memory, owned by the handle until
+ * er_gguf_close) and parses the header, metadata and tensor table.  Data
+ * pointers returned below point into that mapping. */
+typedef struct er_gguf er_gguf;
+ER_API er_status er_gguf_open(const char *path, er_gguf **out);
+ER_API void er_gguf_close(er_gguf *g);
+/* Tensors in the file (-1 for NULL). */
+ER_API int64_t er_gguf_tensor_count(const er_gguf *g);
+/* Tensor i: its NUL-terminated name, GGUF type code (er_dtype values for the
+ * types this library computes with), dimension count, dims[4] (innermost
+ * first: a matrix of `rows` x `cols` has dims {cols, rows, 1, 1}), its bytes in
+ * the mapping and their count.  Any output pointer may be NULL. */
+ER_API er_status er_gguf_tensor_info(const er_gguf *g, int64_t i, const char **name, int32_t *type, int32_t *n_dims,
+                                     int64_t *dims, const void **data, uint64_t *bytes);
+/* Index of the tensor named `name` (ER_EINVAL if absent). */
+ER_API er_status er_gguf_find(const er_gguf *g, const char *name, int64_t *index);
+/* The model shape from the llama.* metadata ("EdgeRunner Core Architecture"
+ * section 1.1: embedding_length, block_count, feed_forward_length,
+ * attention.head_count, attention.head_count_kv (default: head_count),
+ * attention.key_length (default: embedding_length / head_count),
+ * rope.freq_base (default 10000), attention.layer_norm_rms_epsilon (default
+ * 1e-5)); vocab from token_embd.weight; w_type from blk.0.attn_q.weight; tied
+ * when output.weight is absent; max_batch as given.  Every tensor the decode
+ * step reads is checked to exist with the type and shape this implies:
+ * ER_EINVAL (reason in er_last_error) otherwise. */
+ER_API er_status er_gguf_config(const er_gguf *g, int32_t max_batch, er_config *cfg);
+/* er_model_create from the file: the data section is copied to the device
+ * once, handed to er_model_create (which repacks it into model-owned memory)
+ * and freed.  Synchronises `stream`.  The er_gguf may be closed afterwards. */
+ER_API er_status er_model_create_from_gguf(const er_gguf *g, int32_t max_batch, void *stream, er_model **out);
+
 ER_API const char *er_status_str(er_status s);
 ER_API const char *er_last_error(void);
 
