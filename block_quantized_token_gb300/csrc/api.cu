@@ -312,9 +312,6 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
             A(&kv->wide_ssq, ssq * sizeof(float), false);
         }
     }
-    if (e == cudaSuccess)
-        e = attention_tensor_maps(kv->kc, kv->vc, (size_t)batch * c.n_layers * c.n_kv_heads * (size_t)capacity, hd,
-                                  &kv->attn_tmk, &kv->attn_tmv);
     A(&kv->amax, 16 * sizeof(unsigned long long));
     A(&kv->done, sizeof(int));
     A(&kv->flags, sizeof(int));
@@ -504,8 +501,6 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
         }
         case ER_STAGE_ATTN: {
             AttnArgs a = {};
-            a.tmk = kv->attn_tmk;
-            a.tmv = kv->attn_tmv;
             a.q = kv->q;
             a.kc = kv->kc;
             a.vc = kv->vc;

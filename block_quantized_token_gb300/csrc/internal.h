@@ -1,7 +1,6 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -104,10 +103,6 @@ int gemv_max_cols(int qt, int K);  // largest B <= 4 that gemv_fits
 // attention
 // ---------------------------------------------------------------------------
 struct AttnArgs {
-    // 2-D tensor maps over the whole K and V caches: [B * L * KV * cap rows][hd] fp16, boxes of
-    // 16 rows x 64 elements (128 bytes) with the 128-byte swizzle (attention_tensor_maps)
-    CUtensorMap tmk;
-    CUtensorMap tmv;
     const float *q;  // [B][qd]
     const __half *kc, *vc;
     const int32_t *positions;
@@ -119,9 +114,6 @@ struct AttnArgs {
     int B, H, KV, hd, L, layer, cap, S, CH;
 };
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl);
-// encodes the two tensor maps of the attention kernel for a cache of `rows` rows of hd fp16 each
-cudaError_t attention_tensor_maps(const __half *kc, const __half *vc, size_t rows, int hd, CUtensorMap *tmk,
-                                  CUtensorMap *tmv);
 // launch shape of the attention kernel for a cache of this shape
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH);
 size_t attention_part_floats(int hd, int G, int num_sms);  // AttnArgs::part
@@ -251,7 +243,6 @@ struct er_kv {
     float *x, *q, *o, *a;
     float *attn_part;
     int *attn_cnt;
-    CUtensorMap attn_tmk, attn_tmv;  // tensor maps of kc / vc for the attention kernel
     float *gemv_part;
     int *gemv_cnt;
     float *wide_part, *wide_ssq;  // batched GEMV scratch (nullptr: column groups instead)

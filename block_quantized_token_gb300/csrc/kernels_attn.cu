@@ -22,16 +22,13 @@
 //         as hi + lo sums of its accumulator.
 //   O += P V: A = the probabilities in exactly that lane layout (hi rows 0..7,
 //         lo rows 8..15, p = hi + lo); B = V rows (ldmatrix.trans).
-// K and V tiles reach shared memory by tensor TMA (cp.async.bulk.tensor): lane 0
-// of each warp copies a tile as boxes of 16 rows x 64 elements (128 bytes)
-// with the 128-byte swizzle, which stores the 16-byte chunk c of row r of a box
-// at chunk c ^ (r & 7), so the eight rows an ldmatrix reads together sit in
-// eight different bank groups.  Each warp keeps TA_SLOTS tiles in a ring, all
-// but the one it consumes in flight, each completing on its own mbarrier.
+// K and V tiles reach shared memory through cp.async, 16 bytes per lane; the
+// 16-byte chunk c of row r is stored at chunk c ^ (r & 7) of the row, so the
+// eight rows an ldmatrix reads together sit in eight different bank groups.
+// Two tiles per warp are in flight while a third is consumed; a range's first
+// two are requested before its queries are read.
 #include "common.cuh"
 #include "internal.h"
-
-#include <cudaTypedefs.h>
 
 namespace er {
 
@@ -40,33 +37,24 @@ constexpr int TA_SLOTS = 3;
 constexpr int TA_TILE = 16;
 constexpr int TA_MIN_ROWS = 64;  // rows per warp at least
 constexpr int TA_MAXB = 16;
-constexpr int TA_BOX = 64;  // elements per box row (128 bytes: the swizzle span)
 
 template <int HD>
 struct TaCfg {
     static constexpr int KC = HD / 16;                   // k16 chunks of a head (Q K^T)
     static constexpr int NTD = HD / 8;                   // n8 tiles of a head (P V)
-    static constexpr int NBOX = HD / TA_BOX;             // boxes per tile
-    static constexpr int BOXB = TA_TILE * TA_BOX * 2;    // 2048 bytes
-    static constexpr int TILEB = NBOX * BOXB;            // one K or V tile
+    static constexpr int ROWB = HD * 2;                  // row bytes in shared memory (chunks swizzled)
+    static constexpr int TILEB = TA_TILE * ROWB;         // one K or V tile
     static constexpr int SLOT = 2 * TILEB;               // K tile then V tile
-    static constexpr int SMEM = TA_WARPS * TA_SLOTS * SLOT + 1024;  // + alignment of the ring to 1024 bytes
+    static constexpr int CPL = TA_TILE * HD / 8 / 32;    // 16-byte chunks per lane per tile
+    static constexpr int SMEM = TA_WARPS * TA_SLOTS * SLOT;
 };
 
-// tensor-TMA load of one box at element coordinates (x, y), completing on `bar`
-ER_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
+ER_DEV void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-
-// byte offset, inside a tile, of 16-byte chunk c (0 .. HD/8 - 1) of row r
-template <int HD>
-ER_DEV uint32_t ta_chunk(int r, int c) {
-    return (uint32_t)((c >> 3) * TaCfg<HD>::BOXB + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
+ER_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+ER_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 ER_DEV void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -106,33 +94,31 @@ struct TaState {
     float o[TaCfg<HD>::NTD][4];
 };
 
-// Rows [r0, r1) of the cache head whose row 0 is tensor-map row `hrow` for the G
-// query heads at qh (fp32 [G][HD], unscaled).  `ring` (1024-byte aligned) and
-// `bars` (TA_SLOTS mbarriers) are this warp's; `kg` counts the tiles the warp
-// has taken through its ring so far (ring slot and mbarrier phase).  Returns
-// false if a tile wait gave up (flag set, copies drained).
+// Rows [r0, r1) of the cache head at Kb / Vb (row-major [cap][HD]) for the G
+// query heads at qh (fp32 [G][HD], unscaled).
 template <int HD, int G>
-__device__ bool ta_attend(const AttnArgs &a, const float *qh, long long hrow, int r0, int r1, uint8_t *ring,
-                          uint64_t *bars, unsigned &kg, int lane, TaState<HD> &st) {
+__device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, int r0, int r1, uint8_t *ring,
+                          int lane, TaState<HD> &st) {
     using C = TaCfg<HD>;
     const int g = lane >> 2, t = lane & 3;
     const int ntiles = (r1 - r0 + TA_TILE - 1) / TA_TILE;
     const uint32_t ring_s = smem_u32(ring);
-    const unsigned k0 = kg;
-    // lane 0: tile k of this range into ring slot (k0 + k) % TA_SLOTS.  Rows past r1 are
-    // copied too (other rows of the cache, or zeros past its end) and masked below.
     auto issue = [&](int k) {
-        if (lane == 0 && k < ntiles) {
-            const unsigned n = k0 + (unsigned)k, sidx = n % TA_SLOTS;
-            const uint32_t slot = ring_s + sidx * C::SLOT, bar = smem_u32(bars + sidx);
-            const int y = (int)(hrow + r0 + k * TA_TILE);
-            mbar_arrive_expect_tx(bars + sidx, 2 * C::TILEB);
+        if (k < ntiles) {
+            const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
+            const int rb = r0 + k * TA_TILE;
 #pragma unroll
-            for (int bx = 0; bx < C::NBOX; ++bx) {
-                tma_load_2d(slot + bx * C::BOXB, &a.tmk, bx * TA_BOX, y, bar);
-                tma_load_2d(slot + C::TILEB + bx * C::BOXB, &a.tmv, bx * TA_BOX, y, bar);
+            for (int i = 0; i < C::CPL; ++i) {
+                const int ci = lane + 32 * i;            // chunk of the tile
+                const int row = ci / (HD / 8), col = ci % (HD / 8);
+                const bool ok = rb + row < r1;
+                const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 8;
+                const uint32_t d = (uint32_t)(row * C::ROWB + (col ^ (row & 7)) * 16);
+                cp_async16(slot + d, Kb + off, ok ? 16u : 0u);
+                cp_async16(slot + C::TILEB + d, Vb + off, ok ? 16u : 0u);
             }
         }
+        cp_async_commit();  // an empty group keeps the count uniform
     };
     for (int k = 0; k < TA_SLOTS - 1; ++k) issue(k);
     // queries: scale to log2 units, rescale by a power of two so that the lo
@@ -181,45 +167,28 @@ __device__ bool ta_attend(const AttnArgs &a, const float *qh, long long hrow, in
 #pragma unroll
     for (int j = 0; j < C::NTD; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.f;
 
-    // ldmatrix rows of this lane (see the header): K as the B operand (rows
-    // (lane & 7) + 8 (lane >> 4), chunk half (lane >> 3) & 1), V transposed
-    // (rows (lane & 7) + 8 ((lane >> 3) & 1), chunk half lane >> 4)
-    const int k_r = (lane & 7) + ((lane >> 4) << 3), k_half = (lane >> 3) & 1;
-    const int v_r = (lane & 7) + (((lane >> 3) & 1) << 3), v_half = lane >> 4;
-    bool good = true;
-    int k = 0;
-    for (; k < ntiles; ++k) {
+    // ldmatrix row addresses of this lane (see the header): K as the B operand
+    // (rows (lane & 7) + 8 (lane >> 4), column half (lane >> 3) & 1), V
+    // transposed (rows (lane & 7) + 8 ((lane >> 3) & 1), column half lane >> 4)
+    // (the row index mod 8 is lane & 7 in both; chunks are XOR-swizzled by it)
+    const int sw = lane & 7;
+    const uint32_t k_row = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB), k_half = (lane >> 3) & 1;
+    const uint32_t v_row = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB), v_half = lane >> 4;
+    for (int k = 0; k < ntiles; ++k) {
         issue(k + TA_SLOTS - 1);
-        const unsigned n = k0 + (unsigned)k, sidx = n % TA_SLOTS;
-        if (!__all_sync(0xffffffffu, mbar_wait(bars + sidx, (n / TA_SLOTS) & 1u))) {
-            if (lane == 0) atomicOr(a.flags, ER_FLAG_WAIT);
-            good = false;
-            break;
-        }
-        const uint32_t slot = ring_s + sidx * C::SLOT;
-        const int rb = r0 + k * TA_TILE;
-        if (rb + TA_TILE > r1) {
-            // a partial tile: V rows past the range must not meet a zero probability as
-            // non-finite values, so they are zeroed (K rows past it are masked by score)
-            for (int i = lane; i < TA_TILE * (HD / 8); i += 32) {
-                const int r = i / (HD / 8), c = i % (HD / 8);
-                if (rb + r >= r1) {
-                    const uint32_t d = slot + C::TILEB + ta_chunk<HD>(r, c);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(d), "r"(0u) : "memory");
-                }
-            }
-            fence_proxy_async_smem();  // before the slot is refilled by the async proxy
-            __syncwarp();
-        }
+        cp_async_wait<TA_SLOTS - 1>();
+        __syncwarp();
+        const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
         // scores of 16 rows: two n8 tiles (rows 0..7 and 8..15 of the tile)
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < C::KC; ++c) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(slot + ta_chunk<HD>(k_r, 2 * c + k_half), b0, b1, b2, b3);
+            ldsm_x4(slot + k_row + (((2 * c + k_half) ^ sw) << 4), b0, b1, b2, b3);
             mma_16816(s0, qa[c], b0, b1, s0);
             mma_16816(s1, qa[c], b2, b3, s1);
         }
+        const int rb = r0 + k * TA_TILE;
         float sc[4] = {(s0[0] + s0[2]) * down, (s0[1] + s0[3]) * down, (s1[0] + s1[2]) * down,
                        (s1[1] + s1[3]) * down};
         const int rr[4] = {rb + 2 * t, rb + 2 * t + 1, rb + 2 * t + 8, rb + 2 * t + 9};
@@ -256,46 +225,26 @@ __device__ bool ta_attend(const AttnArgs &a, const float *qh, long long hrow, in
 #pragma unroll
         for (int j2 = 0; j2 < C::NTD / 2; ++j2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(slot + C::TILEB + ta_chunk<HD>(v_r, 2 * j2 + v_half), b0, b1, b2, b3);
+            ldsm_x4_t(slot + v_row + (((2 * j2 + v_half) ^ sw) << 4), b0, b1, b2, b3);
             mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
             mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
         }
         __syncwarp();  // every lane is done with this slot before it is refilled
     }
-    // tiles issued are min(ntiles, k + TA_SLOTS - 1 + 1) after k full iterations; after a
-    // give-up, wait (bounded) for those still in flight before the ring is reused or the CTA exits
-    const int issued = ntiles < k + TA_SLOTS ? ntiles : k + TA_SLOTS;
-    kg = k0 + (unsigned)issued;
-    if (!good) {
-        if (lane == 0)
-            for (int j = k; j < issued; ++j)
-                mbar_wait(bars + (k0 + j) % TA_SLOTS, ((k0 + j) / TA_SLOTS) & 1u);
-        return false;
-    }
+    cp_async_wait<0>();
     // the row sum over the four lanes of the head
     st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
     st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
-    return true;
 }
 
 template <int HD, int G>
-__global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArgs a) {
     using C = TaCfg<HD>;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    __shared__ uint64_t bars_s[TA_WARPS * TA_SLOTS];
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
-    // the 128-byte swizzle wants each box at a 1024-byte boundary
-    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t *ring = smem + warp * TA_SLOTS * C::SLOT;
-    uint64_t *bars = bars_s + warp * TA_SLOTS;
     const int qd = a.H * HD;
-    if (lane == 0) {
-        for (int i = 0; i < TA_SLOTS; ++i) mbar_init(bars + i, 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    unsigned kg = 0;  // tiles this warp has taken through its ring
 
     pdl_wait();
     pdl_launch_dependents();
@@ -324,10 +273,10 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const __grid_
         const int r0 = u - seg_start, r1 = (wb < seg_end ? wb : seg_end) - seg_start;
         const bool first_piece = u == wa;
         u = wb < seg_end ? wb : seg_end;
-        const long long hrow = (((long long)b * a.L + a.layer) * a.KV + kvh) * (long long)a.cap;
+        const size_t head_off = (((size_t)b * a.L + a.layer) * a.KV + kvh) * (size_t)a.cap * HD;
         TaState<HD> st;
-        if (!ta_attend<HD, G>(a, a.q + (size_t)b * qd + (size_t)kvh * G * HD, hrow, r0, r1, ring, bars, kg, lane, st))
-            return;  // a tile wait gave up: the flag is set and this warp's copies have landed
+        ta_attend<HD, G>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, a.kc + head_off, a.vc + head_off, r0, r1, ring,
+                         lane, st);
         float *o_grp = a.o + (size_t)b * qd + (size_t)kvh * G * HD;
         if (seg_start >= wa && seg_end <= wb) {  // the whole pair: finish here
             if (g < G) {
@@ -406,32 +355,6 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const __grid_
         }
         if (lane == 0) a.cnt[grp] = 0;
     }
-}
-
-cudaError_t attention_tensor_maps(const __half *kc, const __half *vc, size_t rows, int hd, CUtensorMap *tmk,
-                                  CUtensorMap *tmv) {
-    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-    if (!encode) {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    // [rows][hd] fp16, row stride hd * 2 bytes; boxes of TA_TILE rows x TA_BOX elements; rows
-    // past the end read as zeros
-    const cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)hd * sizeof(__half)};
-    const cuuint32_t box[2] = {TA_BOX, TA_TILE};
-    const cuuint32_t estr[2] = {1, 1};
-    for (int i = 0; i < 2; ++i) {
-        CUresult r = encode(i ? tmv : tmk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)(i ? vc : kc), dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    return cudaSuccess;
 }
 
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH) {
