@@ -38,8 +38,9 @@ template <int QT>
 constexpr int gw_off_operand() { return GW_OFF_RING + GW_WARPS * GW_SLOTS * GvCfg<QT>::SLOT; }
 template <int QT>
 constexpr int gw_smem() {
-    // operand of 32 blocks, then per-column factors [16], column maxima [16] (uint), per-item sums of squares [512]
-    return gw_off_operand<QT>() + 2 * GW_SLICE_UNITS * GW_BLOCK_BYTES + 16 * 4 + 16 * 4 + 512 * 4 + 64;
+    // operand of 32 blocks, then per-column factors [16], per-(warp, segment) maxima [16][8], per-item sums of
+    // squares [512]
+    return gw_off_operand<QT>() + 2 * GW_SLICE_UNITS * GW_BLOCK_BYTES + 16 * 4 + GW_WARPS * 8 * 4 + 512 * 4 + 64;
 }
 
 // first CTA of slice s when C CTAs share S slices
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     uint8_t *op = smem + gw_off_operand<QT>();
     float *fac = reinterpret_cast<float *>(op + 2 * GW_SLICE_UNITS * GW_BLOCK_BYTES);
-    unsigned *cmax = reinterpret_cast<unsigned *>(fac + 16);
-    float *issq = reinterpret_cast<float *>(cmax + 16);
+    float *wmax = fac + 16;  // [warp][i]: largest |x g| of segment warp + 16 i
+    float *issq = wmax + GW_WARPS * 8;
     __shared__ int stop_s;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -188,7 +189,6 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
     // an earlier kernel's give-up flag, read now and published after the operand build, so that
     // nothing waits for this load before then
     const int stop_r = tid == 0 ? (*reinterpret_cast<volatile int *>(a.flags) & ER_FLAG_WAIT) : 0;
-    if (tid < 16) cmax[tid] = 0u;
     // zero the operand columns past the batch (their MMA results are never read, but must be finite)
     const int nbs = (nu * 64) / 32;  // blocks in this slice
     if (2 * a.B < GW_NT * 8)
@@ -198,17 +198,23 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
         }
     __syncthreads();
     // Warps read x in 512-byte segments of one column (lane l: elements 4l .. 4l + 3 of the segment),
-    // so every load instruction touches 4 cache lines.  The 8 lanes of one 32-element block reduce its
-    // sum of squares and largest |x g| by shuffles; lane 8i writes them.
+    // so every load instruction touches 4 cache lines; the gain's elements are requested with them.
+    // The 8 lanes of one 32-element block reduce its sum of squares by shuffles (lane 8i writes it),
+    // and the warp reduces the segment's largest |x g| (lane 0 writes it): no shared-memory atomics.
     const int nel = nu * 64, spc = (nel + 127) / 128, nseg = a.B * spc;  // segments per column, in all
     float v[8][4];
+    float4 gv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int seg = warp + GW_WARPS * i;
         const int b = seg / spc, e0 = (seg - b * spc) * 128 + 4 * lane;  // element of the slice
         const bool live = seg < nseg && e0 < nel;
         float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (live) x4 = __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.K + ku0 * 64 + e0));
+        gv[i] = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (live) {
+            x4 = __ldcg(reinterpret_cast<const float4 *>(a.x + (size_t)b * a.K + ku0 * 64 + e0));
+            if (a.gain) gv[i] = __ldg(reinterpret_cast<const float4 *>(a.gain + ku0 * 64 + e0));
+        }
         v[i][0] = x4.x; v[i][1] = x4.y; v[i][2] = x4.z; v[i][3] = x4.w;
     }
 #pragma unroll
@@ -221,30 +227,24 @@ __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvA
         if (live) {
 #pragma unroll
             for (int c = 0; c < 4; ++c) ssq = fmaf(v[i][c], v[i][c], ssq);
-            if (a.gain) {
-                const float4 g4 = __ldg(reinterpret_cast<const float4 *>(a.gain + ku0 * 64 + e0));
-                v[i][0] *= g4.x; v[i][1] *= g4.y; v[i][2] *= g4.z; v[i][3] *= g4.w;
-            }
+            v[i][0] *= gv[i].x; v[i][1] *= gv[i].y; v[i][2] *= gv[i].z; v[i][3] *= gv[i].w;
 #pragma unroll
             for (int c = 0; c < 4; ++c) m = fmaxf(m, fabsf(v[i][c]));
         }
 #pragma unroll
-        for (int off = 1; off < 8; off <<= 1) {
-            ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        }
-        if (live && (lane & 7) == 0) {
-            issq[(e0 >> 5) * a.B + b] = ssq;
-            if (!isfinite(m)) m = 0.f;
-            atomicMax(cmax + b, __float_as_uint(m));  // non-negative floats order as their bits
-        }
+        for (int off = 1; off < 8; off <<= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (live && (lane & 7) == 0) issq[(e0 >> 5) * a.B + b] = ssq;
+        if (lane == 0) wmax[warp * 8 + i] = isfinite(m) ? m : 0.f;
     }
     __syncthreads();
     if (tid < a.B) {
         float t = 0.f;
         for (int i = tid; i < nbs * a.B; i += a.B) t += issq[i];  // block order: deterministic
         wssq[s * 16 + tid] = t;  // every CTA of the slice writes the same value
-        const float mx = __uint_as_float(cmax[tid]);
+        float mx = 0.f;  // the column's segments are tid * spc .. tid * spc + spc - 1
+        for (int sg = tid * spc; sg < (tid + 1) * spc; ++sg) mx = fmaxf(mx, wmax[(sg % GW_WARPS) * 8 + sg / GW_WARPS]);
         int e = 0;
         if (mx > 0.f) {
             int E;
