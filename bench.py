@@ -252,13 +252,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     # kernel's own duration; the outer pair times the whole chain
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if args.flush_l2 else None
+    # a read of 256 MiB (larger than L2) between steps leaves L2 holding only clean lines, so no
+    # write-back of the flush itself lands inside the next step's timing
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev) if args.flush_l2 else None
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         ev0.record(stream)
         for i in range(K):
-            if flush is not None:  # a write larger than L2 between steps (outside the per-step events)
-                flush.fill_(i & 0xFF)
+            if flush is not None:  # a read larger than L2 between steps (outside the per-step events)
+                flush.sum()
             evs[i][0].record(stream)
             er.er_decode_step(tok.data_ptr(), pos.data_ptr(), state.handle, logits.data_ptr(), tok.data_ptr(), sp)
             evs[i][1].record(stream)
@@ -362,13 +364,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
 def stage_roofline(er, state, wl, tok, pos, logits, stream, dev, iters: int = 20) -> dict:
     """Average event-timed duration of each stage kernel at the workload's first position.
 
-    Every launch is preceded by a write of a 256 MiB buffer (larger than L2), so
-    the weights come from HBM as in the chained step.  Returns the roofline of
-    the stage with the largest total time per step.
+    Every launch is preceded by a read of a 256 MiB buffer (larger than L2), so
+    the weights come from HBM as in the chained step.  A read, not a write: a
+    written buffer would leave up to an L2's worth of dirty lines whose
+    write-back lands inside the timed launch.  Returns the roofline of the
+    stage with the largest total time per step.
     """
     import torch
     peaks = measured_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     pos_np = wl.positions0()
     sb = stage_bytes(wl, pos_np)
     L = wl.shape.n_layers
@@ -383,7 +387,7 @@ def stage_roofline(er, state, wl, tok, pos, logits, stream, dev, iters: int = 20
         for name, sid in ids.items():
             tot = 0.0
             for i in range(iters + 2):
-                flush.fill_(i & 0xFF)
+                flush.sum()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 er.er_launch_stage(state.handle, sid, L // 2, tok.data_ptr(), pos.data_ptr(), logits.data_ptr(),
@@ -462,7 +466,7 @@ def oracle_sample(wl: synth.Workload, steps: int, budget_s: float, seqs=None) ->
 
 def gemv_sweep(reps: int = 50) -> dict:
     """The isolated Q4_0 GEMV sweep of the 135M-shaped Q4_0 workload: M x K = 576x576, 1536x576, 49152x576,
-    batch 1, through er_matrix_gemv.  Each launch follows a 256 MiB write (larger than L2), so the weights come
+    batch 1, through er_matrix_gemv.  Each launch follows a 256 MiB read (larger than L2), so the weights come
     from HBM; CUDA events around each launch on the launching stream."""
     import torch
     from block_quantized_token_gb300 import build as libbuild
@@ -470,7 +474,7 @@ def gemv_sweep(reps: int = 50) -> dict:
         libbuild.build()
     from block_quantized_token_gb300 import er
     peaks = measured_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")  # read, not written: no dirty lines
     stream = torch.cuda.Stream()
     out = {}
     for rows, cols in ((576, 576), (1536, 576), (49152, 576)):
@@ -483,7 +487,7 @@ def gemv_sweep(reps: int = 50) -> dict:
         tot = 0.0
         with torch.cuda.stream(stream):
             for i in range(reps + 3):
-                flush.fill_(i & 0xFF)
+                flush.sum()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
                 er.er_matrix_gemv(m, x.data_ptr(), 1, y.data_ptr(), stream.cuda_stream)
@@ -506,7 +510,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--flush-l2", action="store_true",
-                    help="write 256 MiB between steps and time the step graphs alone (for L2-sized workloads)")
+                    help="read 256 MiB between steps and time the step graphs alone (for L2-sized workloads)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--gemv-sweep", action="store_true",
                     help="time the isolated Q4_0 GEMV sweep (576x576, 1536x576, 49152x576) and print it")
