@@ -23,6 +23,7 @@ decoding.  The whole-step composition beyond those pins is "parity unpinned":
 the pages print no logits for any model.
 """
 
-from .blocks import BLOCK_BYTES, dequant, dequant_q4_0, dequant_q8_0, dequant_rows  # noqa: F401
+from .blocks import (BLOCK_BYTES, dequant, dequant_kv_q8_0, dequant_q4_0, dequant_q8_0, dequant_rows,  # noqa: F401
+                     quantize_kv_q8_0)
 from .ops import attention_gqa, matvec, rmsnorm, rope, silu, softmax, swiglu  # noqa: F401
 from .decode import OracleCache, OracleConfig, OracleModel, decode_step, greedy, uncached_logits  # noqa: F401

@@ -70,3 +70,39 @@ def dequant_rows(raw: np.ndarray, kind: str, rows: int, cols: int, idx) -> np.nd
     idx = np.atleast_1d(np.asarray(idx, dtype=np.int64))
     sub = np.asarray(raw).reshape(rows, -1)[idx]
     return dequant(sub, kind, len(idx), cols)
+
+
+def quantize_kv_q8_0(x) -> tuple[np.ndarray, np.ndarray]:
+    """Quantise cache rows to Q8_0 blocks: x float32 [..., n] (n a multiple of 32) -> (d fp16 [..., n/32],
+    q int8 [..., n]).
+
+    The pages store K/V optionally as packed Q8_0 ("llama.cpp Metal (MPS) End-to-End Inference Path", P9
+    quantized-KV flash-attention variants and section 5, minfer's packed Q8_0 cache; "EdgeRunner Core
+    Architecture" section 4.1, cache precision options) but give no quantiser for the cache.  The reading
+    here: the Q8_0 rule of the weights (scale = largest |x| / 127, q = round(x / scale)) with the division by
+    the scale as stored, so that d * q is the stored value, and every step in float32, the precision the
+    kernel takes the decision in:
+      amax = max |x_j|                      (exact)
+      d    = fp16(float32(amax / 127))      (float32 division, then round to nearest even in fp16)
+      q_j  = clamp(round(float32(x_j / d)), -127, 127), round half away from zero; q = 0 when d = 0.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    if x.shape[-1] % QK:
+        raise ValueError("rows must be whole blocks of 32")
+    xb = x.reshape(x.shape[:-1] + (x.shape[-1] // QK, QK))
+    amax = np.max(np.abs(xb), axis=-1)
+    d = (amax / np.float32(127.0)).astype(np.float32).astype(np.float16)
+    d32 = d.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.where(d32[..., None] > 0, xb / d32[..., None], np.float32(0.0)).astype(np.float32)
+    q = np.sign(r) * np.floor(np.abs(r) + np.float32(0.5))
+    q = np.clip(q, -127, 127).astype(np.int8)
+    return d, q.reshape(x.shape)
+
+
+def dequant_kv_q8_0(d, q) -> np.ndarray:
+    """d fp16 [..., n/32], q int8 [..., n] -> float64 [..., n]: value = d * q (exact)."""
+    d = np.asarray(d, dtype=np.float16).astype(np.float64)
+    q = np.asarray(q, dtype=np.int8).astype(np.float64)
+    qb = q.reshape(q.shape[:-1] + (q.shape[-1] // QK, QK))
+    return (d[..., None] * qb).reshape(q.shape)

@@ -22,7 +22,10 @@ Readings where the pages are silent (each listed in the design notes):
   * cached K rows are post-RoPE keys; V is not rotated;
   * argmax ties go to the lowest index, NaN never wins, any non-finite logit
     sets the flag;
-  * prefilled cache rows are given, already in cache form (fp16).
+  * prefilled cache rows are given, already in cache form (fp16);
+  * a Q8_0 cache (OracleCache kv_type "q8_0", an option the pages name without
+    a quantiser) stores each head's row as Q8_0 blocks quantised by
+    blocks.quantize_kv_q8_0, and attention reads d * q.
 """
 
 from __future__ import annotations
@@ -32,7 +35,7 @@ from typing import Callable, Mapping
 
 import numpy as np
 
-from .blocks import dequant, dequant_rows
+from .blocks import dequant, dequant_kv_q8_0, dequant_rows, quantize_kv_q8_0
 from .ops import attention_gqa, matvec, rmsnorm, rope, swiglu
 
 
@@ -121,20 +124,47 @@ class OracleModel:
 
 
 class OracleCache:
-    """fp16 K and V rows per (sequence, layer): arrays [capacity, n_kv_heads, head_dim]."""
+    """K and V rows per (sequence, layer): arrays [capacity, n_kv_heads, head_dim].
 
-    def __init__(self, cfg: OracleConfig, batch: int, capacity: int):
-        self.cfg, self.batch, self.capacity = cfg, batch, capacity
+    kv_type "f16" (the pages' default cache precision): the rows are fp16.
+    kv_type "q8_0": each head's row is stored as Q8_0 blocks (blocks.quantize_kv_q8_0); k / v then hold
+    the dequantised values d * q (exact in float32) and kd / kq / vd / vq the blocks themselves.
+    """
+
+    def __init__(self, cfg: OracleConfig, batch: int, capacity: int, kv_type: str = "f16"):
+        if kv_type not in ("f16", "q8_0"):
+            raise ValueError(kv_type)
+        self.cfg, self.batch, self.capacity, self.kv_type = cfg, batch, capacity, kv_type
         shp = (capacity, cfg.n_kv_heads, cfg.head_dim)
-        self.k = [[np.zeros(shp, np.float16) for _ in range(cfg.n_layers)] for _ in range(batch)]
-        self.v = [[np.zeros(shp, np.float16) for _ in range(cfg.n_layers)] for _ in range(batch)]
+        dt = np.float16 if kv_type == "f16" else np.float32
+        self.k = [[np.zeros(shp, dt) for _ in range(cfg.n_layers)] for _ in range(batch)]
+        self.v = [[np.zeros(shp, dt) for _ in range(cfg.n_layers)] for _ in range(batch)]
+        if kv_type == "q8_0":
+            dshp = (capacity, cfg.n_kv_heads, cfg.head_dim // 32)
+            self.kd = [[np.zeros(dshp, np.float16) for _ in range(cfg.n_layers)] for _ in range(batch)]
+            self.vd = [[np.zeros(dshp, np.float16) for _ in range(cfg.n_layers)] for _ in range(batch)]
+            self.kq = [[np.zeros(shp, np.int8) for _ in range(cfg.n_layers)] for _ in range(batch)]
+            self.vq = [[np.zeros(shp, np.int8) for _ in range(cfg.n_layers)] for _ in range(batch)]
+
+    def put(self, b: int, layer: int, rows: slice | int, k, v) -> None:
+        """Store K and V values [..., n_kv_heads, head_dim] at `rows` in the cache's precision."""
+        if self.kv_type == "f16":
+            self.k[b][layer][rows] = np.asarray(k, np.float64).astype(np.float16)
+            self.v[b][layer][rows] = np.asarray(v, np.float64).astype(np.float16)
+            return
+        for vals, full, ds, qs in ((k, self.k, self.kd, self.kq), (v, self.v, self.vd, self.vq)):
+            d, q = quantize_kv_q8_0(np.asarray(vals, np.float64).astype(np.float32))
+            ds[b][layer][rows] = d
+            qs[b][layer][rows] = q
+            full[b][layer][rows] = dequant_kv_q8_0(d, q).astype(np.float32)
 
     def fill(self, b: int, layer: int, k_rows: np.ndarray, v_rows: np.ndarray, start: int = 0) -> None:
-        """Copy token-major rows [n, n_kv_heads*head_dim] into rows start..start+n-1."""
+        """Store token-major fp16 rows [n, n_kv_heads*head_dim] at rows start..start+n-1."""
         n = k_rows.shape[0]
         c = self.cfg
-        self.k[b][layer][start:start + n] = np.asarray(k_rows, np.float16).reshape(n, c.n_kv_heads, c.head_dim)
-        self.v[b][layer][start:start + n] = np.asarray(v_rows, np.float16).reshape(n, c.n_kv_heads, c.head_dim)
+        k = np.asarray(k_rows, np.float16).reshape(n, c.n_kv_heads, c.head_dim)
+        v = np.asarray(v_rows, np.float16).reshape(n, c.n_kv_heads, c.head_dim)
+        self.put(b, layer, slice(start, start + n), k, v)
 
 
 def _argmax_flag(logits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
@@ -168,8 +198,7 @@ def decode_step(model: OracleModel, cache: OracleCache, tokens, positions,
             pb = int(pos[i])
             qh = rope(q[i].reshape(c.n_heads, c.head_dim), pb, c.rope_base)
             kh = rope(k[i].reshape(c.n_kv_heads, c.head_dim), pb, c.rope_base)
-            cache.k[b][l][pb] = kh.astype(np.float16)
-            cache.v[b][l][pb] = v[i].reshape(c.n_kv_heads, c.head_dim).astype(np.float16)
+            cache.put(b, l, pb, kh, v[i].reshape(c.n_kv_heads, c.head_dim))
             o[i] = attention_gqa(qh, cache.k[b][l][:pb + 1], cache.v[b][l][:pb + 1]).reshape(-1)
         x = x + matvec(model.matrix(p + "attn_output.weight"), o)
         h2 = rmsnorm(x, model.gain(p + "ffn_norm.weight"), c.rms_eps)
@@ -199,11 +228,12 @@ def greedy(model: OracleModel, cache: OracleCache, tokens, positions, steps: int
     return np.array(fed), np.array(out)
 
 
-def uncached_logits(model: OracleModel, token_seq) -> np.ndarray:
+def uncached_logits(model: OracleModel, token_seq, kv_type: str = "f16") -> np.ndarray:
     """Logits at the last position of `token_seq` (positions 0..n-1) recomputed from scratch.
 
-    Every position's K and V are computed together, rounded to fp16 as the
-    cache would hold them, and each query attends to positions 0..itself.
+    Every position's K and V are computed together, rounded as a cache of
+    `kv_type` would hold them (fp16, or Q8_0 blocks), and each query attends to
+    positions 0..itself.
     Used to check incremental decoding ("cached == uncached", alpaca.swift README,
     "Numerical validation", levels 2-4).
     """
@@ -218,8 +248,12 @@ def uncached_logits(model: OracleModel, token_seq) -> np.ndarray:
         k = matvec(model.matrix(p + "attn_k.weight"), h)
         v = matvec(model.matrix(p + "attn_v.weight"), h)
         K = np.stack([rope(k[t].reshape(c.n_kv_heads, c.head_dim), t, c.rope_base) for t in range(n)])
-        K = K.astype(np.float16)
-        V = v.reshape(n, c.n_kv_heads, c.head_dim).astype(np.float16)
+        V = v.reshape(n, c.n_kv_heads, c.head_dim)
+        if kv_type == "f16":
+            K, V = K.astype(np.float16), V.astype(np.float16)
+        else:
+            K = dequant_kv_q8_0(*quantize_kv_q8_0(K.astype(np.float32)))
+            V = dequant_kv_q8_0(*quantize_kv_q8_0(V.astype(np.float32)))
         o = np.stack([attention_gqa(rope(q[t].reshape(c.n_heads, c.head_dim), t, c.rope_base),
                                     K[:t + 1], V[:t + 1]).reshape(-1) for t in range(n)])
         x = x + matvec(model.matrix(p + "attn_output.weight"), o)

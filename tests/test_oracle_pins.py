@@ -348,6 +348,59 @@ def check_greedy(shape=TINY):
             seq.append(int(np.argmax(want)))
 
 
+def check_kv_q8_0():
+    """The Q8_0 cache quantizer: hand-derived blocks and the bound every block satisfies.
+
+    - 0.5 * (integers up to 127): the scale 63.5 / 127 = 0.5 is exact, the round trip is exact.
+    - a block of largest |x| = 127 (scale 1): 2.5 -> 3 and -2.5 -> -3 (ties away from zero), 0.49 -> 0.
+    - a block of largest |x| = 100: 100 / 127 = 0.787401... is stored as fp16 1613 * 2^-11 = 0.78759765625;
+      50 / 0.78759765625 = 63.484... -> 63 (dividing by the unrounded scale would give 63.5 -> 64), and the
+      largest element 100 / 0.78759765625 = 126.97 -> 127.
+    - an all-zero block stores d = 0, q = 0.
+    - random blocks: |x - d q| <= d / 2 + 2^-20 |x| element-wise, |q| <= 127, and the largest element maps
+      to +-127.
+    """
+    qz = oracle.blocks.quantize_kv_q8_0
+    x = np.zeros(64, np.float32)
+    x[:32] = 0.5 * (np.arange(32) * 8 - 127).clip(-127, 127)
+    d, q = qz(x)
+    assert d[0] == np.float16(0.5) and d[1] == 0 and not q[32:].any()
+    np.testing.assert_array_equal(oracle.blocks.dequant_kv_q8_0(d, q), x.astype(np.float64))
+    blk = np.zeros(32, np.float32)
+    blk[:4] = [127.0, 2.5, -2.5, 0.49]
+    d, q = qz(blk)
+    assert d[0] == np.float16(1.0) and list(q[:4]) == [127, 3, -3, 0]
+    blk = np.zeros(32, np.float32)
+    blk[:2] = [100.0, 50.0]
+    d, q = qz(blk)
+    assert float(d[0]) == 1613 * 2.0 ** -11 and list(q[:2]) == [127, 63]
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((50, 128)) * rng.uniform(0.01, 100, (50, 1))).astype(np.float32)
+    d, q = qz(x)
+    assert np.abs(q.astype(int)).max() <= 127
+    dd = np.repeat(d.astype(np.float64), 32, axis=-1)
+    err = np.abs(x.astype(np.float64) - oracle.blocks.dequant_kv_q8_0(d, q))
+    assert (err <= dd / 2 + 2.0 ** -20 * np.abs(x)).all()
+    xb, qb = x.reshape(50, 4, 32), q.reshape(50, 4, 32)
+    top = np.argmax(np.abs(xb), axis=-1)
+    assert (np.abs(np.take_along_axis(qb, top[..., None], -1)) == 127).all()
+
+
+TINY_HD32 = synth.ModelShape(**{**TINY.__dict__, "n_heads": 2, "n_kv_heads": 1, "head_dim": 32})
+
+
+def check_cached_equals_uncached_q8(shape=TINY_HD32):
+    """With a Q8_0 cache, incremental decoding equals the from-scratch recompute that quantises K and V the
+    same way (head rows of whole 32-element blocks)."""
+    model = oracle_model(shape)
+    toks = [3, 17, 99, 5, 64]
+    cache = oracle.OracleCache(oracle_config(shape), 1, len(toks), kv_type="q8_0")
+    for n, t in enumerate(toks):
+        logits, _, _ = oracle.decode_step(model, cache, [t], [n])
+        np.testing.assert_allclose(logits[0], oracle.uncached_logits(model, toks[:n + 1], kv_type="q8_0"),
+                                   rtol=1e-11, atol=1e-13)
+
+
 def check_argmax():
     lg = np.array([[1.0, 3.0, 3.0, -np.inf], [np.nan, 0.5, 0.5, 0.1], [np.inf, 2.0, np.inf, 1.0]])
     am, nf = oracle.decode._argmax_flag(lg)
@@ -359,7 +412,8 @@ def check_argmax():
 
 # ------------------------------------------------------------------------------------------
 PINS = [check_block_sizes, check_q8_0_hand_blocks, check_q4_0_hand_blocks, check_quantize_roundtrip, check_matvec,
-        check_rmsnorm, check_rope, check_softmax, check_attention, check_silu, check_argmax]
+        check_rmsnorm, check_rope, check_softmax, check_attention, check_silu, check_argmax, check_kv_q8_0,
+        check_cached_equals_uncached_q8]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -466,6 +520,26 @@ def _greedy_variant(stuck_position: bool, wrong_slot: bool):
     return run
 
 
+def _kvq_unrounded(x):
+    """The cache quantizer dividing by the unrounded scale."""
+    x = np.asarray(x, np.float32)
+    xb = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    s = (np.max(np.abs(xb), axis=-1) / np.float32(127)).astype(np.float32)
+    r = np.where(s[..., None] > 0, xb / np.where(s > 0, s, 1)[..., None], 0).astype(np.float32)
+    q = np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+    return s.astype(np.float16), q.reshape(x.shape)
+
+
+def _kvq_half_even(x):
+    """The cache quantizer rounding ties to even."""
+    d, _ = oracle.blocks.__dict__["_orig_quantize_kv_q8_0"](x)
+    x = np.asarray(x, np.float32)
+    xb = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+    d32 = d.astype(np.float32)
+    r = np.where(d32[..., None] > 0, xb / np.where(d32 > 0, d32, 1)[..., None], 0).astype(np.float32)
+    return d, np.clip(np.rint(r), -127, 127).astype(np.int8).reshape(x.shape)
+
+
 MISTAKES = [
     ("blocks", "dequant_q4_0", _q4_swapped, check_q4_0_hand_blocks),
     ("blocks", "dequant_q8_0", _q8_unsigned, check_q8_0_hand_blocks),
@@ -476,6 +550,8 @@ MISTAKES = [
     ("ops", "rmsnorm", _rms_eps_out, check_rmsnorm),
     ("ops", "silu", _silu_sigmoid, check_silu),
     ("ops", "matvec", _matvec_T, check_matvec),
+    ("blocks", "quantize_kv_q8_0", _kvq_unrounded, check_kv_q8_0),
+    ("blocks", "quantize_kv_q8_0", _kvq_half_even, check_kv_q8_0),
     ("decode", "greedy", _greedy_variant(True, False), check_greedy),
     ("decode", "greedy", _greedy_variant(False, True), check_greedy),
 ]
