@@ -95,7 +95,10 @@ def quantize_kv_q8_0(x) -> tuple[np.ndarray, np.ndarray]:
     d32 = d.astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
         r = np.where(d32[..., None] > 0, xb / d32[..., None], np.float32(0.0)).astype(np.float32)
-    q = np.sign(r) * np.floor(np.abs(r) + np.float32(0.5))
+    # round the float32 quotient half away from zero; the addition is exact in float64 (in float32 it
+    # would round a quotient just below one half, such as 0.49999997, up to 1)
+    r64 = r.astype(np.float64)
+    q = np.sign(r64) * np.floor(np.abs(r64) + 0.5)
     q = np.clip(q, -127, 127).astype(np.int8)
     return d, q.reshape(x.shape)
 

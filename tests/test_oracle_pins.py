@@ -352,7 +352,8 @@ def check_kv_q8_0():
     """The Q8_0 cache quantizer: hand-derived blocks and the bound every block satisfies.
 
     - 0.5 * (integers up to 127): the scale 63.5 / 127 = 0.5 is exact, the round trip is exact.
-    - a block of largest |x| = 127 (scale 1): 2.5 -> 3 and -2.5 -> -3 (ties away from zero), 0.49 -> 0.
+    - a block of largest |x| = 127 (scale 1): 2.5 -> 3 and -2.5 -> -3 (ties away from zero), 0.49 -> 0, and
+      the largest float32 below one half -> 0.
     - a block of largest |x| = 100: 100 / 127 = 0.787401... is stored as fp16 1613 * 2^-11 = 0.78759765625;
       50 / 0.78759765625 = 63.484... -> 63 (dividing by the unrounded scale would give 63.5 -> 64), and the
       largest element 100 / 0.78759765625 = 126.97 -> 127.
@@ -367,9 +368,9 @@ def check_kv_q8_0():
     assert d[0] == np.float16(0.5) and d[1] == 0 and not q[32:].any()
     np.testing.assert_array_equal(oracle.blocks.dequant_kv_q8_0(d, q), x.astype(np.float64))
     blk = np.zeros(32, np.float32)
-    blk[:4] = [127.0, 2.5, -2.5, 0.49]
+    blk[:5] = [127.0, 2.5, -2.5, 0.49, np.nextafter(np.float32(0.5), np.float32(0))]
     d, q = qz(blk)
-    assert d[0] == np.float16(1.0) and list(q[:4]) == [127, 3, -3, 0]
+    assert d[0] == np.float16(1.0) and list(q[:5]) == [127, 3, -3, 0, 0]
     blk = np.zeros(32, np.float32)
     blk[:2] = [100.0, 50.0]
     d, q = qz(blk)
