@@ -55,10 +55,16 @@ def stage_bytes(wl: synth.Workload, pos: np.ndarray) -> dict[str, float]:
     D, qd, kvd, F, V = s.dim, s.qd, s.kvd, s.ffn_dim, s.vocab
     w = matrix_bytes(s)
     attn_rows = float(np.sum(pos + 1))
+    if wl.kv_type == "q8_0":
+        # per row and side kvd / 32 blocks of 34 bytes; the new rows go through fp32 staging (written by the
+        # QKV GEMV, read by the quantiser) before their blocks are written
+        kv_row, kv_new = kvd / 32 * 34, kvd * 4 * 2 + kvd / 32 * 34
+    else:
+        kv_row, kv_new = kvd * 2, kvd * 2
     return {
         "embed": B * D * (2.0 if not s.tied else bpb) + B * D * 4,
-        "qkv": w["qkv"] + B * (D * 4 + qd * 4 + 2 * kvd * 2) + D * 4,
-        "attn": attn_rows * kvd * 2 * 2 + B * qd * 4 * 2,
+        "qkv": w["qkv"] + B * (D * 4 + qd * 4 + 2 * kv_new) + D * 4,
+        "attn": attn_rows * kv_row * 2 + B * qd * 4 * 2,
         "wo": w["wo"] + B * (qd * 4 + 2 * D * 4),
         "gateup": w["gateup"] + B * (D * 4 + F * 4) + D * 4,
         "down": w["down"] + B * (F * 4 + 2 * D * 4),
@@ -207,7 +213,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     t0 = time.time()
     threads = min(32, os.cpu_count() or 1)
     model = runtime.DecodeModel(s, synth.model_weights(s, threads=threads), max_batch=B)
-    state = runtime.DecodeState(model, B, cap)
+    state = runtime.DecodeState(model, B, cap, kv_type=wl.kv_type)
     from concurrent.futures import ThreadPoolExecutor
     with ThreadPoolExecutor(max_workers=threads) as ex:  # draws run in parallel, writes in order
         jobs = [(b, l) for b in range(B) for l in range(s.n_layers)]
@@ -343,7 +349,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             "config": {"workload": wl.name, "model": f"{s.n_layers}L d{s.dim} {s.n_heads}/{s.n_kv_heads}x{s.head_dim} "
                                                      f"ffn{s.ffn_dim} V{s.vocab} {s.w_type} "
                                                      f"{'tied' if s.tied else 'untied'}",
-                       "batch": B, "context": wl.prefill, "chained_steps": K, "schedule": schedule,
+                       "batch": B, "context": wl.prefill, "kv_cache": wl.kv_type, "chained_steps": K, "schedule": schedule,
                        "step_bytes": bytes_step, "step_gbs": bytes_step / (ms / K / 1e3) / 1e9,
                        "step_roofline_frac": bytes_step / (ms / K / 1e3) / 1e9 / measured_peaks()["hbm_gbs"],
                        "step_frac_of_8tbs": bytes_step / (ms / K / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -421,7 +427,7 @@ def _oracle_run(wl: synth.Workload, n_layers: int, steps: int, budget_s: float, 
     wk = wl.with_(shape=s)
     tensors = synth.model_weights(s)
     ocfg = oracle.OracleConfig(**{k: getattr(s, k) for k in oracle.OracleConfig.__dataclass_fields__})
-    cache = oracle.OracleCache(ocfg, wl.batch, wl.prefill + steps)
+    cache = oracle.OracleCache(ocfg, wl.batch, wl.prefill + steps, kv_type=wl.kv_type)
     for b in seqs:
         for l in range(n_layers):
             k, v = synth.kv_prefill(wk, b, l)
@@ -549,7 +555,7 @@ def main():
         line = {"metric": METRIC, "value": tps, "unit": "tok/s", "n_gpus": args.gpus, "steps": done,
                 "warmup": 0, "ms_per_step": info["seconds"] * 1e3 / max(done, 1), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": wl.name, "batch": wl.batch, "context": wl.prefill},
+                "config": {"workload": wl.name, "batch": wl.batch, "context": wl.prefill, "kv_cache": wl.kv_type},
                 "impl": "reference",
                 "cpu_baseline": {"value": tps, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": sample},
                 "e2e": {"value": tps, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

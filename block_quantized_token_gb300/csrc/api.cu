@@ -251,14 +251,23 @@ size_t er_model_device_bytes(const er_model *m) { return m ? m->device_bytes : 0
 // decode state
 // ---------------------------------------------------------------------------
 er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out) {
+    return er_kv_create_typed(m, batch, capacity, ER_F16, out);
+}
+
+er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32_t kv_type, er_kv **out) {
     if (!m || !out) return fail(ER_EINVAL, "NULL argument");
     const er_config &c = m->cfg;
     if (batch < 1 || batch > c.max_batch) return fail(ER_EINVAL, "batch must be in 1..max_batch");
     if (capacity < 1 || capacity > (1 << 24)) return fail(ER_EINVAL, "capacity out of range");
+    if (kv_type != ER_F16 && kv_type != ER_Q8_0) return fail(ER_EINVAL, "kv_type must be ER_F16 or ER_Q8_0");
     er_kv *kv = new er_kv();
     kv->m = m;
     kv->B = batch;
     kv->cap = capacity;
+    kv->kv_type = kv_type;
+    kv->kc = kv->vc = nullptr;
+    kv->kvq = {};
+    kv->kstage = kv->vstage = nullptr;
     kv->cap_stream = nullptr;
     kv->graph_calls = 0;
     kv->bar_extra = 0;
@@ -279,8 +288,20 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
         e = dalloc(kv->allocs, p, bytes);
         if (e == cudaSuccess && zero) e = cudaMemset(*p, 0, bytes);
     };
-    A(&kv->kc, cache_elems * sizeof(__half));
-    A(&kv->vc, cache_elems * sizeof(__half));
+    if (kv_type == ER_F16) {
+        A(&kv->kc, cache_elems * sizeof(__half));
+        A(&kv->vc, cache_elems * sizeof(__half));
+    } else {
+        A(&kv->kvq.kq, cache_elems);
+        A(&kv->kvq.vq, cache_elems);
+        A(&kv->kvq.kd, cache_elems / 32 * sizeof(__half));
+        A(&kv->kvq.vd, cache_elems / 32 * sizeof(__half));
+        kv->kvq.L = c.n_layers;
+        kv->kvq.KV = c.n_kv_heads;
+        kv->kvq.cap = capacity;
+        A(&kv->kstage, (size_t)batch * kvd * sizeof(float));
+        A(&kv->vstage, (size_t)batch * kvd * sizeof(float));
+    }
     A(&kv->rope, (size_t)capacity * (hd / 2) * sizeof(float2), false);
     A(&kv->x, (size_t)batch * D * sizeof(float));
     A(&kv->q, (size_t)batch * qd * sizeof(float));
@@ -335,8 +356,8 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
             R[i] = mats[i]->R;
             UPR[i] = mats[i]->UPR;
         }
-        kv->step_ok = e == cudaSuccess && step_supported(c.w_type, hd, G, batch, c.n_kv_heads, capacity, max_k, R, UPR,
-                                                         m->num_sms);
+        kv->step_ok = e == cudaSuccess && kv_type == ER_F16 &&
+                      step_supported(c.w_type, hd, G, batch, c.n_kv_heads, capacity, max_k, R, UPR, m->num_sms);
         kv->schedule = kv->step_ok ? ER_SCHEDULE_PERSISTENT : ER_SCHEDULE_KERNELS;
         A(&kv->step_layers, (size_t)c.n_layers * sizeof(StepLayer), false);
         A(&kv->step_apart, step_apart_floats(m->num_sms, hd) * sizeof(float), false);
@@ -376,8 +397,11 @@ void er_kv_destroy(er_kv *kv) {
     delete kv;
 }
 
+int32_t er_kv_type(const er_kv *kv) { return kv ? kv->kv_type : -1; }
+
 er_status er_kv_layer_ptrs(er_kv *kv, int32_t seq, int32_t layer, void **k_dev, void **v_dev) {
     if (!kv || !k_dev || !v_dev) return fail(ER_EINVAL, "NULL argument");
+    if (kv->kv_type != ER_F16) return fail(ER_EUNSUPPORTED, "the cache holds Q8_0 blocks, not fp16 rows");
     const er_config &c = kv->m->cfg;
     if (seq < 0 || seq >= kv->B || layer < 0 || layer >= c.n_layers) return fail(ER_EINVAL, "seq or layer out of range");
     size_t off = ((size_t)seq * c.n_layers + layer) * (size_t)c.n_kv_heads * kv->cap * c.head_dim;
@@ -394,6 +418,11 @@ static er_status kv_copy(er_kv *kv, int seq, int layer, int start, int n, bool w
     if (n < 0 || start < 0 || (long long)start + n > kv->cap) return fail(ER_EINVAL, "rows out of range");
     if (n == 0) return ER_OK;
     const int hd = c.head_dim, kvd = c.n_kv_heads * hd;
+    if (kv->kv_type == ER_Q8_0) {
+        if (!write) return fail(ER_EUNSUPPORTED, "the cache holds Q8_0 blocks: read them with er_kv_read_blocks");
+        ER_CUDA(launch_kvq_write((const __half *)k, (const __half *)v, n, kv->kvq, hd, seq, layer, start, st));
+        return ER_OK;
+    }
     size_t base = ((size_t)seq * c.n_layers + layer) * (size_t)c.n_kv_heads * kv->cap * hd;
     for (int h = 0; h < c.n_kv_heads; ++h) {
         __half *ck = kv->kc + base + ((size_t)h * kv->cap + start) * hd;
@@ -420,6 +449,19 @@ er_status er_kv_write(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int3
 er_status er_kv_read(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n, void *k, void *v,
                      void *stream) {
     return kv_copy(kv, seq, layer, start, n, false, k, v, (cudaStream_t)stream);
+}
+
+er_status er_kv_read_blocks(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n, void *k_blocks,
+                            void *v_blocks, void *stream) {
+    if (!kv || !k_blocks || !v_blocks) return fail(ER_EINVAL, "NULL argument");
+    if (kv->kv_type != ER_Q8_0) return fail(ER_EUNSUPPORTED, "the cache holds fp16 rows: read them with er_kv_read");
+    const er_config &c = kv->m->cfg;
+    if (seq < 0 || seq >= kv->B || layer < 0 || layer >= c.n_layers) return fail(ER_EINVAL, "seq or layer out of range");
+    if (n < 0 || start < 0 || (long long)start + n > kv->cap) return fail(ER_EINVAL, "rows out of range");
+    if (n == 0) return ER_OK;
+    ER_CUDA(launch_kvq_read((uint8_t *)k_blocks, (uint8_t *)v_blocks, n, kv->kvq, c.head_dim, seq, layer, start,
+                            (cudaStream_t)stream));
+    return ER_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -497,13 +539,22 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
             a.L = c.n_layers;
             a.layer = l;
             a.cap = kv->cap;
-            return gemv_all(kv, EPI_QKV, a, st, pdl);
+            a.k_stage = kv->kstage;  // Q8_0 cache: fp32 rows, quantised by the next launch
+            a.v_stage = kv->vstage;
+            cudaError_t e = gemv_all(kv, EPI_QKV, a, st, pdl);
+            if (e == cudaSuccess && kv->kv_type == ER_Q8_0)
+                e = launch_kvq_stage(kv->kstage, kv->vstage, positions, kv->B, kv->kvq, c.head_dim, l, st, pdl);
+            return e;
         }
         case ER_STAGE_ATTN: {
             AttnArgs a = {};
             a.q = kv->q;
             a.kc = kv->kc;
             a.vc = kv->vc;
+            a.kq = kv->kvq.kq;  // nullptr on an fp16 cache
+            a.vq = kv->kvq.vq;
+            a.kd = kv->kvq.kd;
+            a.vd = kv->kvq.vd;
             a.positions = positions;
             a.o = kv->o;
             a.part = kv->attn_part;
@@ -727,7 +778,8 @@ int32_t er_kv_launches_per_step(const er_kv *kv) {
         return per > 0 ? (kv->B + per - 1) / per : 0;
     };
     const er_layer_dev &L0 = m->layers[0];
-    const int per_layer = groups(L0.qkv) + 1 + groups(L0.wo) + groups(L0.gateup) + groups(L0.down);
+    const int per_layer = groups(L0.qkv) + (kv->kv_type == ER_Q8_0 ? 1 : 0) + 1 + groups(L0.wo) + groups(L0.gateup) +
+                          groups(L0.down);
     return 1 + c.n_layers * per_layer + groups(m->head);
 }
 

@@ -198,15 +198,23 @@ __device__ inline void gv_epilogue(const GemvArgs &a, int rg, float v0, float v1
                 float2 *q = reinterpret_cast<float2 *>(a.q_out + (size_t)bt * a.qd + r0);
                 *q = make_float2(o0, o1);
             } else {
-                int kvh = base / a.hd;
-                size_t off = ((((size_t)bt * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
-                *reinterpret_cast<__half2 *>(a.kc + off) = __floats2half2_rn(o0, o1);
+                if (a.k_stage) {
+                    *reinterpret_cast<float2 *>(a.k_stage + (size_t)bt * a.kvd + base) = make_float2(o0, o1);
+                } else {
+                    int kvh = base / a.hd;
+                    size_t off = ((((size_t)bt * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
+                    *reinterpret_cast<__half2 *>(a.kc + off) = __floats2half2_rn(o0, o1);
+                }
             }
         } else {
             int base = r0 - a.qd - a.kvd;
-            int kvh = base / a.hd, dd = base % a.hd;
-            size_t off = ((((size_t)bt * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
-            *reinterpret_cast<__half2 *>(a.vc + off) = __floats2half2_rn(v0, v1);
+            if (a.v_stage) {
+                *reinterpret_cast<float2 *>(a.v_stage + (size_t)bt * a.kvd + base) = make_float2(v0, v1);
+            } else {
+                int kvh = base / a.hd, dd = base % a.hd;
+                size_t off = ((((size_t)bt * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
+                *reinterpret_cast<__half2 *>(a.vc + off) = __floats2half2_rn(v0, v1);
+            }
         }
     } else if (EPI == EPI_SWIGLU) {
         if (!bok) return;

@@ -54,6 +54,7 @@ struct GemvArgs {
     // QKV epilogue
     float *q_out;
     __half *kc, *vc;
+    float *k_stage, *v_stage;  // non-null: K/V rows go to fp32 staging [batch][kvd] instead of kc / vc
     const float2 *rope;
     const int32_t *positions;
     int qd, kvd, hd, KV, L, layer, cap;
@@ -104,7 +105,9 @@ int gemv_max_cols(int qt, int K);  // largest B <= 4 that gemv_fits
 // ---------------------------------------------------------------------------
 struct AttnArgs {
     const float *q;  // [B][qd]
-    const __half *kc, *vc;
+    const __half *kc, *vc;        // fp16 cache [B][L][KV][cap][hd], or
+    const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): values [B][L][KV][cap][hd]
+    const __half *kd, *vd;        //   and block scales [B][L][KV][cap][hd / 32]
     const int32_t *positions;
     float *o;  // [B][qd]
     float *part;  // warp states of pairs shared by warps (attention_part_floats)
@@ -114,6 +117,25 @@ struct AttnArgs {
     int B, H, KV, hd, L, layer, cap, S, CH;
 };
 cudaError_t launch_attention(const AttnArgs &a, cudaStream_t st, bool pdl);
+
+// ---------------------------------------------------------------------------
+// Q8_0 K/V cache (kernels_kvq.cu): values [B][L][KV][cap][hd] int8 and block
+// scales [B][L][KV][cap][hd / 32] fp16, one plane pair for K and one for V
+// ---------------------------------------------------------------------------
+struct KvqCache {
+    int8_t *kq, *vq;
+    __half *kd, *vd;
+    int L, KV, cap;
+};
+// fp16 token-major rows [n][KV * hd] (device) -> cache rows start.. of (seq, layer)
+cudaError_t launch_kvq_write(const __half *k_rows, const __half *v_rows, int n, const KvqCache &c, int hd, int seq,
+                             int layer, int start, cudaStream_t st);
+// the step's fp32 staging rows [B][KV * hd] -> cache row positions[b] of `layer`
+cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const int32_t *positions, int B,
+                             const KvqCache &c, int hd, int layer, cudaStream_t st, bool pdl);
+// cache rows start.. of (seq, layer) -> GGUF Q8_0 blocks [n][KV * hd / 32][34] (device)
+cudaError_t launch_kvq_read(uint8_t *k_out, uint8_t *v_out, int n, const KvqCache &c, int hd, int seq, int layer,
+                            int start, cudaStream_t st);
 // launch shape of the attention kernel for a cache of this shape
 void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH);
 size_t attention_part_floats(int hd, int G, int num_sms);  // AttnArgs::part
@@ -238,7 +260,10 @@ struct er_kv {
     float *step_apart;
     int *step_acnt;
     unsigned *step_bar;
-    __half *kc, *vc;
+    int kv_type;                 // ER_KV_F16 or ER_KV_Q8_0
+    __half *kc, *vc;             // fp16 cache (ER_KV_F16)
+    er::KvqCache kvq;            // Q8_0 cache (ER_KV_Q8_0)
+    float *kstage, *vstage;      // Q8_0: the step's new K/V rows in fp32 [B][kvd]
     float2 *rope;
     float *x, *q, *o, *a;
     float *attn_part;

@@ -49,6 +49,29 @@ struct TaCfg {
     static constexpr int SMEM = TA_WARPS * TA_SLOTS * SLOT;
 };
 
+// Q8_0 cache tiles (kernels_kvq.cu layout): per slot the K and V tiles' quantised bytes [TA_TILE][HD] and
+// scales [TA_TILE][HD / 32]; each warp also has one fp16 tile pair (K, V) in the fp16 path's layout, into
+// which it converts the quantised values (exact) before the tensor-core products.
+template <int HD>
+struct TaQ8Cfg {
+    static constexpr int QT = TA_TILE * HD;             // quantised bytes of one tile
+    static constexpr int SROW = HD / 32 * 2;            // scale bytes of one row: 8 or 4
+    static constexpr int ST = TA_TILE * SROW;           // scale bytes of one tile
+    static constexpr int SLOT = 2 * (QT + ST);          // K then V: bytes, then scales
+    static constexpr int SLOTS = TA_SLOTS;              // tiles staged per warp
+    static constexpr int CONV = 2 * TaCfg<HD>::TILEB;   // the warp's converted fp16 K and V tiles
+    static constexpr int WARP = SLOTS * SLOT + CONV;
+    static constexpr int SMEM = TA_WARPS * WARP;
+    static constexpr float VPRE = 256.f;  // power of two the V-scaled probabilities are multiplied by
+};
+
+ER_DEV void cp_async_ca(uint32_t dst, const void *src, uint32_t src_bytes, int size) {
+    if (size == 8)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
 ER_DEV void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -94,33 +117,63 @@ struct TaState {
     float o[TaCfg<HD>::NTD][4];
 };
 
-// Rows [r0, r1) of the cache head at Kb / Vb (row-major [cap][HD]) for the G
-// query heads at qh (fp32 [G][HD], unscaled).
-template <int HD, int G>
-__device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, int r0, int r1, uint8_t *ring,
-                          int lane, TaState<HD> &st) {
+// One (sequence, KV head) of the cache: fp16 rows K, V ([cap][HD]), or Q8_0 planes Kq, Vq ([cap][HD] int8)
+// with scales Kd, Vd ([cap][HD / 32] fp16).
+struct TaSrc {
+    const __half *K, *V;
+    const int8_t *Kq, *Vq;
+    const __half *Kd, *Vd;
+};
+
+// Rows [r0, r1) of the cache head `src` for the G query heads at qh (fp32 [G][HD], unscaled).  Q8: the
+// cache holds Q8_0 blocks.
+template <int HD, int G, bool Q8>
+__device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uint8_t *ring, int lane,
+                          TaState<HD> &st) {
     using C = TaCfg<HD>;
+    using Q = TaQ8Cfg<HD>;
     const int g = lane >> 2, t = lane & 3;
     const int ntiles = (r1 - r0 + TA_TILE - 1) / TA_TILE;
     const uint32_t ring_s = smem_u32(ring);
+    constexpr int NS = Q8 ? Q::SLOTS : TA_SLOTS;  // ring slots
     auto issue = [&](int k) {
         if (k < ntiles) {
-            const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
             const int rb = r0 + k * TA_TILE;
+            if constexpr (!Q8) {
+                const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
 #pragma unroll
-            for (int i = 0; i < C::CPL; ++i) {
-                const int ci = lane + 32 * i;            // chunk of the tile
-                const int row = ci / (HD / 8), col = ci % (HD / 8);
-                const bool ok = rb + row < r1;
-                const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 8;
-                const uint32_t d = (uint32_t)(row * C::ROWB + (col ^ (row & 7)) * 16);
-                cp_async16(slot + d, Kb + off, ok ? 16u : 0u);
-                cp_async16(slot + C::TILEB + d, Vb + off, ok ? 16u : 0u);
+                for (int i = 0; i < C::CPL; ++i) {
+                    const int ci = lane + 32 * i;            // chunk of the tile
+                    const int row = ci / (HD / 8), col = ci % (HD / 8);
+                    const bool ok = rb + row < r1;
+                    const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 8;
+                    const uint32_t d = (uint32_t)(row * C::ROWB + (col ^ (row & 7)) * 16);
+                    cp_async16(slot + d, src.K + off, ok ? 16u : 0u);
+                    cp_async16(slot + C::TILEB + d, src.V + off, ok ? 16u : 0u);
+                }
+            } else {
+                // quantised bytes: 16-byte chunks, row-major [TA_TILE][HD]; scales: one copy per row
+                const uint32_t slot = ring_s + (uint32_t)((k % NS) * Q::SLOT);
+#pragma unroll
+                for (int i = 0; i < Q::QT / 16 / 32; ++i) {
+                    const int ci = lane + 32 * i, row = ci / (HD / 16), col = ci % (HD / 16);
+                    const bool ok = rb + row < r1;
+                    const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 16;
+                    cp_async16(slot + ci * 16, src.Kq + off, ok ? 16u : 0u);
+                    cp_async16(slot + Q::QT + Q::ST + ci * 16, src.Vq + off, ok ? 16u : 0u);
+                }
+                if (lane < 2 * TA_TILE) {
+                    const int row = lane & (TA_TILE - 1), kv = lane >> 4;
+                    const bool ok = rb + row < r1;
+                    const size_t off = (size_t)(ok ? rb + row : r0) * (HD / 32);
+                    cp_async_ca(slot + kv * (Q::QT + Q::ST) + Q::QT + row * Q::SROW, (kv ? src.Vd : src.Kd) + off,
+                                ok ? (uint32_t)Q::SROW : 0u, Q::SROW);
+                }
             }
         }
         cp_async_commit();  // an empty group keeps the count uniform
     };
-    for (int k = 0; k < TA_SLOTS - 1; ++k) issue(k);
+    for (int k = 0; k < NS - 1; ++k) issue(k);
     // queries: scale to log2 units, rescale by a power of two so that the lo
     // halves stay normal, split hi + lo into A fragments
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);
@@ -174,19 +227,79 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
     const int sw = lane & 7;
     const uint32_t k_row = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB), k_half = (lane >> 3) & 1;
     const uint32_t v_row = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB), v_half = lane >> 4;
+    const uint32_t conv = ring_s + NS * Q::SLOT;  // Q8: this warp's converted fp16 tiles
     for (int k = 0; k < ntiles; ++k) {
-        issue(k + TA_SLOTS - 1);
-        cp_async_wait<TA_SLOTS - 1>();
+        issue(k + NS - 1);
+        cp_async_wait<NS - 1>();
         __syncwarp();
-        const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
-        // scores of 16 rows: two n8 tiles (rows 0..7 and 8..15 of the tile)
+        uint32_t slot;
         float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        // Q8: the K/V scales of this lane's four rows 2t, 2t + 1, 2t + 8, 2t + 9 (fp16 pairs)
+        uint32_t dks[4][HD / 64], dvs[4][HD / 64];
+        if constexpr (!Q8) {
+            slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
+            // scores of 16 rows: two n8 tiles (rows 0..7 and 8..15 of the tile)
 #pragma unroll
-        for (int c = 0; c < C::KC; ++c) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(slot + k_row + (((2 * c + k_half) ^ sw) << 4), b0, b1, b2, b3);
-            mma_16816(s0, qa[c], b0, b1, s0);
-            mma_16816(s1, qa[c], b2, b3, s1);
+            for (int c = 0; c < C::KC; ++c) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(slot + k_row + (((2 * c + k_half) ^ sw) << 4), b0, b1, b2, b3);
+                mma_16816(s0, qa[c], b0, b1, s0);
+                mma_16816(s1, qa[c], b2, b3, s1);
+            }
+        } else {
+            const uint32_t qslot = ring_s + (uint32_t)((k % NS) * Q::SLOT);
+            // the quantised K and V tiles into fp16 (exact), in the fp16 path's swizzled layout
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+                for (int i = 0; i < Q::QT / 16 / 32; ++i) {
+                    const int ci = lane + 32 * i, row = ci / (HD / 16), col = ci % (HD / 16);
+                    const uint4 w = lds128(qslot + kv * (Q::QT + Q::ST) + ci * 16);
+                    uint32_t h[8];
+                    q8_word_to_h2(w.x ^ 0x80808080u, h[0], h[1]);
+                    q8_word_to_h2(w.y ^ 0x80808080u, h[2], h[3]);
+                    q8_word_to_h2(w.z ^ 0x80808080u, h[4], h[5]);
+                    q8_word_to_h2(w.w ^ 0x80808080u, h[6], h[7]);
+                    const uint32_t base = conv + kv * C::TILEB + row * C::ROWB;
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + (((2 * col) ^ (row & 7)) << 4)),
+                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + (((2 * col + 1) ^ (row & 7)) << 4)),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+                }
+            const int rows4[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int w = 0; w < HD / 64; ++w) {
+                    uint32_t x;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(qslot + Q::QT + rows4[i] * Q::SROW + 4 * w));
+                    dks[i][w] = x;
+                    asm volatile("ld.shared.u32 %0, [%1];"
+                                 : "=r"(x)
+                                 : "r"(qslot + Q::QT + Q::ST + Q::QT + rows4[i] * Q::SROW + 4 * w));
+                    dvs[i][w] = x;
+                }
+            __syncwarp();
+            slot = conv;
+            // scores block by block (2 k16 chunks per 32-value block), each block's sums times its row's scale
+#pragma unroll
+            for (int bb = 0; bb < HD / 32; ++bb) {
+                float b0s[4] = {0.f, 0.f, 0.f, 0.f}, b1s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 2 * bb; c < 2 * bb + 2; ++c) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(slot + k_row + (((2 * c + k_half) ^ sw) << 4), b0, b1, b2, b3);
+                    mma_16816(b0s, qa[c], b0, b1, b0s);
+                    mma_16816(b1s, qa[c], b2, b3, b1s);
+                }
+                float dk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) dk[i] = (bb & 1) ? h2f_hi(dks[i][bb >> 1]) : h2f_lo(dks[i][bb >> 1]);
+                s0[0] = fmaf(dk[0], b0s[0], s0[0]); s0[2] = fmaf(dk[0], b0s[2], s0[2]);
+                s0[1] = fmaf(dk[1], b0s[1], s0[1]); s0[3] = fmaf(dk[1], b0s[3], s0[3]);
+                s1[0] = fmaf(dk[2], b1s[0], s1[0]); s1[2] = fmaf(dk[2], b1s[2], s1[2]);
+                s1[1] = fmaf(dk[3], b1s[1], s1[1]); s1[3] = fmaf(dk[3], b1s[3], s1[3]);
+            }
         }
         const int rb = r0 + k * TA_TILE;
         float sc[4] = {(s0[0] + s0[2]) * down, (s0[1] + s0[3]) * down, (s1[0] + s1[2]) * down,
@@ -214,36 +327,68 @@ __device__ void ta_attend(const float *qh, const __half *Kb, const __half *Vb, i
             for (int i = 0; i < 4; ++i) p[i] = exp2f(sc[i] - mn);
             st.l += (p[0] + p[1]) + (p[2] + p[3]);
         }
-        float ph[4], pl[4];
+        if constexpr (!Q8) {
+            float ph[4], pl[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ph[i] = __half2float(__float2half_rn(p[i]));
-            pl[i] = p[i] - ph[i];
-        }
-        const uint32_t pa[4] = {pack_h2(ph[0], ph[1]), pack_h2(pl[0], pl[1]), pack_h2(ph[2], ph[3]),
-                                pack_h2(pl[2], pl[3])};
+            for (int i = 0; i < 4; ++i) {
+                ph[i] = __half2float(__float2half_rn(p[i]));
+                pl[i] = p[i] - ph[i];
+            }
+            const uint32_t pa[4] = {pack_h2(ph[0], ph[1]), pack_h2(pl[0], pl[1]), pack_h2(ph[2], ph[3]),
+                                    pack_h2(pl[2], pl[3])};
 #pragma unroll
-        for (int j2 = 0; j2 < C::NTD / 2; ++j2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(slot + v_row + (((2 * j2 + v_half) ^ sw) << 4), b0, b1, b2, b3);
-            mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
-            mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
+            for (int j2 = 0; j2 < C::NTD / 2; ++j2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(slot + v_row + (((2 * j2 + v_half) ^ sw) << 4), b0, b1, b2, b3);
+                mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
+                mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
+            }
+        } else {
+            // per 32-value block of V: P times the block's row scales (and 2^8, so that the fp16 halves
+            // stay normal), split hi + lo, against the block's four n8 tiles
+#pragma unroll
+            for (int bb = 0; bb < HD / 32; ++bb) {
+                float ph[4], pl[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float dv = (bb & 1) ? h2f_hi(dvs[i][bb >> 1]) : h2f_lo(dvs[i][bb >> 1]);
+                    const float pv = p[i] * dv * Q::VPRE;
+                    ph[i] = __half2float(__float2half_rn(pv));
+                    pl[i] = pv - ph[i];
+                }
+                const uint32_t pa[4] = {pack_h2(ph[0], ph[1]), pack_h2(pl[0], pl[1]), pack_h2(ph[2], ph[3]),
+                                        pack_h2(pl[2], pl[3])};
+#pragma unroll
+                for (int j2 = 2 * bb; j2 < 2 * bb + 2; ++j2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(slot + v_row + (((2 * j2 + v_half) ^ sw) << 4), b0, b1, b2, b3);
+                    mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
+                    mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
+                }
+            }
         }
         __syncwarp();  // every lane is done with this slot before it is refilled
     }
     cp_async_wait<0>();
+    if constexpr (Q8) {  // undo the probabilities' power-of-two factor
+#pragma unroll
+        for (int j = 0; j < C::NTD; ++j) {
+            st.o[j][0] *= 1.f / Q::VPRE; st.o[j][1] *= 1.f / Q::VPRE;
+            st.o[j][2] *= 1.f / Q::VPRE; st.o[j][3] *= 1.f / Q::VPRE;
+        }
+    }
     // the row sum over the four lanes of the head
     st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
     st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
 }
 
-template <int HD, int G>
+template <int HD, int G, bool Q8>
 __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArgs a) {
     using C = TaCfg<HD>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
-    uint8_t *ring = smem + warp * TA_SLOTS * C::SLOT;
+    uint8_t *ring = smem + warp * (Q8 ? TaQ8Cfg<HD>::WARP : TA_SLOTS * C::SLOT);
     const int qd = a.H * HD;
 
     pdl_wait();
@@ -273,10 +418,22 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArg
         const int r0 = u - seg_start, r1 = (wb < seg_end ? wb : seg_end) - seg_start;
         const bool first_piece = u == wa;
         u = wb < seg_end ? wb : seg_end;
-        const size_t head_off = (((size_t)b * a.L + a.layer) * a.KV + kvh) * (size_t)a.cap * HD;
+        const size_t head = ((size_t)b * a.L + a.layer) * a.KV + kvh;
+        TaSrc src;
+        if constexpr (Q8) {
+            src.K = src.V = nullptr;
+            src.Kq = a.kq + head * a.cap * HD;
+            src.Vq = a.vq + head * a.cap * HD;
+            src.Kd = a.kd + head * a.cap * (HD / 32);
+            src.Vd = a.vd + head * a.cap * (HD / 32);
+        } else {
+            src.K = a.kc + head * a.cap * HD;
+            src.V = a.vc + head * a.cap * HD;
+            src.Kq = src.Vq = nullptr;
+            src.Kd = src.Vd = nullptr;
+        }
         TaState<HD> st;
-        ta_attend<HD, G>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, a.kc + head_off, a.vc + head_off, r0, r1, ring,
-                         lane, st);
+        ta_attend<HD, G, Q8>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, src, r0, r1, ring, lane, st);
         float *o_grp = a.o + (size_t)b * qd + (size_t)kvh * G * HD;
         if (seg_start >= wa && seg_end <= wb) {  // the whole pair: finish here
             if (g < G) {
@@ -367,17 +524,19 @@ size_t attention_part_floats(int hd, int G, int num_sms) { return (size_t)num_sm
 
 template <int HD, int G>
 static cudaError_t at_launch(const AttnArgs &a, cudaStream_t st, bool pdl) {
+    const bool q8 = a.kq != nullptr;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3((unsigned)a.S);
     cfg.blockDim = dim3(TA_WARPS * 32);
-    cfg.dynamicSmemBytes = TaCfg<HD>::SMEM;
+    cfg.dynamicSmemBytes = q8 ? TaQ8Cfg<HD>::SMEM : TaCfg<HD>::SMEM;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, G>, a);
+    if (q8) return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, G, true>, a);
+    return cudaLaunchKernelEx(&cfg, attn_tc_kernel<HD, G, false>, a);
 }
 
 template <int HD>
@@ -395,14 +554,20 @@ static cudaError_t at_launch_g(const AttnArgs &a, cudaStream_t st, bool pdl) {
     return cudaErrorInvalidValue;
 }
 
-template <int HD, int G>
-static cudaError_t at_attr() {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TaCfg<HD>::SMEM);
+template <int HD, int G, bool Q8>
+static cudaError_t at_attr1() {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Q8 ? TaQ8Cfg<HD>::SMEM : TaCfg<HD>::SMEM);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attn_tc_kernel<HD, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(attn_tc_kernel<HD, G, Q8>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
     return e;
+}
+
+template <int HD, int G>
+static cudaError_t at_attr() {
+    const cudaError_t e = at_attr1<HD, G, false>();
+    return e != cudaSuccess ? e : at_attr1<HD, G, true>();
 }
 
 cudaError_t attention_prepare() {

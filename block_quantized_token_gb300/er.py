@@ -57,6 +57,9 @@ def _load() -> ctypes.CDLL:
         "er_model_destroy": (None, [VP]),
         "er_model_device_bytes": (ctypes.c_size_t, [VP]),
         "er_kv_create": (I32, [VP, I32, I32, P(VP)]),
+        "er_kv_create_typed": (I32, [VP, I32, I32, I32, P(VP)]),
+        "er_kv_type": (I32, [VP]),
+        "er_kv_read_blocks": (I32, [VP, I32, I32, I32, I32, VP, VP, VP]),
         "er_kv_destroy": (None, [VP]),
         "er_kv_layer_ptrs": (I32, [VP, I32, I32, P(VP), P(VP)]),
         "er_kv_write": (I32, [VP, I32, I32, I32, I32, VP, VP, VP]),
@@ -108,7 +111,8 @@ EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_
             "er_kv_launches_per_step", "er_kv_cached_graphs", "er_kv_inject_wait_shortfall", "er_set_wait_limit_ns",
             "er_debug_fail_allocation", "er_debug_live_allocations", "er_gguf_open", "er_gguf_close",
             "er_gguf_tensor_count", "er_gguf_tensor_info", "er_gguf_find", "er_gguf_config",
-            "er_model_create_from_gguf", "er_status_str", "er_last_error")
+            "er_model_create_from_gguf", "er_kv_create_typed", "er_kv_type", "er_kv_read_blocks", "er_status_str",
+            "er_last_error")
 
 
 def lib() -> ctypes.CDLL:
@@ -147,6 +151,21 @@ def er_kv_create(model: int, batch: int, capacity: int) -> int:
     out = ctypes.c_void_p()
     _check(_lib.er_kv_create(model, batch, capacity, ctypes.byref(out)), "er_kv_create")
     return out.value
+
+
+def er_kv_create_typed(model: int, batch: int, capacity: int, kv_type: int) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.er_kv_create_typed(model, batch, capacity, kv_type, ctypes.byref(out)), "er_kv_create_typed")
+    return out.value
+
+
+def er_kv_type(kv: int | None) -> int:
+    return _lib.er_kv_type(kv)
+
+
+def er_kv_read_blocks(kv: int, seq: int, layer: int, start: int, n: int, k_blocks: int, v_blocks: int,
+                      stream: int = 0) -> None:
+    _check(_lib.er_kv_read_blocks(kv, seq, layer, start, n, k_blocks, v_blocks, stream), "er_kv_read_blocks")
 
 
 def er_kv_destroy(kv: int) -> None:

@@ -21,6 +21,9 @@ _LAYER_FIELDS = (("attn_norm", "attn_norm"), ("wq", "attn_q"), ("wk", "attn_k"),
                  ("w_down", "ffn_down"))
 
 
+KV_TYPES = {"f16": er.DTYPES["f16"], "q8_0": er.DTYPES["q8_0"]}  # er_kv_create_typed storage codes
+
+
 def make_config(shape, max_batch: int = 1) -> er.er_config:
     """er_config from any object with the ModelShape fields."""
     return er.er_config(dim=shape.dim, n_layers=shape.n_layers, n_heads=shape.n_heads, n_kv_heads=shape.n_kv_heads,
@@ -76,9 +79,13 @@ class DecodeModel:
 class DecodeState:
     """Owns an er_kv (KV cache + scratch of `batch` sequences) of a DecodeModel."""
 
-    def __init__(self, model: DecodeModel, batch: int, capacity: int):
+    def __init__(self, model: DecodeModel, batch: int, capacity: int, kv_type: str = "f16"):
+        """kv_type "f16" (fp16 rows) or "q8_0" (packed Q8_0 blocks, quantised as rows are written)."""
         self.model, self.batch, self.capacity = model, batch, capacity
-        self.handle = er.er_kv_create(model.handle, batch, capacity)
+        if kv_type not in KV_TYPES:
+            raise ValueError(f"kv_type must be one of {sorted(KV_TYPES)}")
+        self.kv_type = kv_type
+        self.handle = er.er_kv_create_typed(model.handle, batch, capacity, KV_TYPES[kv_type])
 
     def write_rows(self, seq: int, layer: int, k_rows: np.ndarray | torch.Tensor, v_rows, start: int = 0,
                    stream: int | None = None) -> None:
@@ -99,6 +106,24 @@ class DecodeState:
         er.er_kv_read(self.handle, seq, layer, start, n, k.data_ptr(), v.data_ptr(), st)
         torch.cuda.current_stream(self.model.device).synchronize()
         return k, v
+
+    def read_blocks(self, seq: int, layer: int, start: int, n: int) -> tuple[np.ndarray, np.ndarray]:
+        """Q8_0 cache rows start..start+n-1 as GGUF blocks: (d fp16, q int8) per side, shaped
+        [n, n_kv_heads*head_dim/32] and [n, n_kv_heads*head_dim]."""
+        s = self.model.shape
+        nb = s.n_kv_heads * s.head_dim // 32
+        k = torch.empty((n, nb, 34), dtype=torch.uint8, device=self.model.device)
+        v = torch.empty_like(k)
+        st = torch.cuda.current_stream(self.model.device).cuda_stream
+        er.er_kv_read_blocks(self.handle, seq, layer, start, n, k.data_ptr(), v.data_ptr(), st)
+        torch.cuda.current_stream(self.model.device).synchronize()
+        out = []
+        for t in (k, v):
+            a = t.cpu().numpy()
+            d = np.ascontiguousarray(a[:, :, :2]).view(np.float16).reshape(n, nb)
+            q = np.ascontiguousarray(a[:, :, 2:]).view(np.int8).reshape(n, nb * 32)
+            out += [d, q]
+        return tuple(out)
 
     def step(self, tokens: torch.Tensor, positions: torch.Tensor, logits: torch.Tensor | None,
              argmax: torch.Tensor | None, graph: bool = True, stream: int | None = None) -> None:

@@ -112,16 +112,51 @@ ER_API size_t er_model_device_bytes(const er_model *m);
 ER_API er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out);
 ER_API void er_kv_destroy(er_kv *kv);
 
+/* er_kv_create with a choice of cache storage, kv_type:
+ *   ER_F16   the fp16 cache of er_kv_create
+ *   ER_Q8_0  a packed Q8_0 cache: each head's row of head_dim values is kept as
+ *            head_dim / 32 blocks of one fp16 scale d and 32 int8 codes q, and
+ *            attention reads d * q.  The pages list a packed Q8_0 K/V cache as
+ *            an option ("llama.cpp Metal (MPS) End-to-End Inference Path",
+ *            table P9, the quantised-KV flash-attention variant, and the KV
+ *            format note of its section 5) without giving its quantiser; the one
+ *            used here, for every row written (er_kv_write and the step's new
+ *            rows), in float32: amax = max |x| over the block,
+ *            d = fp16(amax / 127) (round to nearest even),
+ *            q = round(x / d) half away from zero, clamped to [-127, 127],
+ *            q = 0 where d = 0.  A step's new K/V rows are quantised from the
+ *            fp32 projection (after RoPE for K); er_kv_write quantises fp16 rows.
+ *            Runs the per-phase schedule only (ER_SCHEDULE_PERSISTENT is
+ *            ER_EUNSUPPORTED); head_dim 64 or 128.  Cache bytes per row and KV
+ *            head: 2 * 34 * head_dim / 32 (K and V), against 4 * head_dim.
+ * Any other kv_type is ER_EINVAL. */
+ER_API er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32_t kv_type, er_kv **out);
+/* The cache storage of kv (ER_F16 or ER_Q8_0), or -1 for NULL. */
+ER_API int32_t er_kv_type(const er_kv *kv);
+
+/* Reads cache rows start..start+n-1 of sequence `seq`, layer `layer` of an
+ * ER_Q8_0 cache as GGUF Q8_0 blocks: k_blocks_dev / v_blocks_dev receive
+ * [n][n_kv_heads * head_dim / 32] blocks of 34 bytes (little-endian fp16 d,
+ * then 32 int8 q), token-major with heads contiguous, n * n_kv_heads *
+ * head_dim / 32 * 34 bytes each (device memory the caller owns).  Queued on
+ * `stream`.  ER_EUNSUPPORTED on an fp16 cache; ER_EINVAL for rows out of
+ * range. */
+ER_API er_status er_kv_read_blocks(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n,
+                                   void *k_blocks_dev, void *v_blocks_dev, void *stream);
+
 /* Device addresses of the K and V cache of sequence `seq`, layer `layer`.
  * Layout of each: fp16 [n_kv_heads][capacity][head_dim] (head-major, then
  * position, then dimension).  K rows hold keys after RoPE; V rows are not
- * rotated.  Callers prefill rows below a sequence's first position here. */
+ * rotated.  Callers prefill rows below a sequence's first position here.
+ * ER_EUNSUPPORTED on an ER_Q8_0 cache. */
 ER_API er_status er_kv_layer_ptrs(er_kv *kv, int32_t seq, int32_t layer, void **k_dev, void **v_dev);
 
 /* Copy n token-major rows k_rows_dev / v_rows_dev (fp16 [n][n_kv_heads*head_dim],
  * heads contiguous within a row, the layout GGUF runtimes use) into cache rows
  * start..start+n-1 of sequence `seq`, layer `layer` (er_kv_write), or the
- * reverse (er_kv_read).  Queued on `stream`; no synchronisation. */
+ * reverse (er_kv_read).  Queued on `stream`; no synchronisation.  On an
+ * ER_Q8_0 cache er_kv_write quantises the rows (er_kv_create_typed) and
+ * er_kv_read is ER_EUNSUPPORTED (er_kv_read_blocks reads the blocks). */
 ER_API er_status er_kv_write(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n, const void *k_rows_dev,
                              const void *v_rows_dev, void *stream);
 ER_API er_status er_kv_read(er_kv *kv, int32_t seq, int32_t layer, int32_t start, int32_t n, void *k_rows_dev,
@@ -178,7 +213,8 @@ ER_API er_status er_kv_set_wide_gemv(er_kv *kv, int32_t variant);
 /* Kernel launches one er_decode_step enqueues under the schedule in effect
  * (memsets not counted), or -1 for NULL: 1 for the persistent schedule; for
  * the per-phase one, the embedding, per layer the QKV, attention, Wo, gate/up
- * and down launches, and the head.  A GEMV is one launch for batches up to 4
+ * and down launches (and, on an ER_Q8_0 cache, the quantisation of the new
+ * K/V rows), and the head.  A GEMV is one launch for batches up to 4
  * and for batches of 5..16 whose matrices take the one-pass batched kernel
  * (K a multiple of 64); otherwise one launch per group of at most 4 batch
  * columns that fit its shared memory. */

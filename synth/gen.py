@@ -47,6 +47,7 @@ class Workload:
     steps: int
     prefill: int
     first_token: int = 7
+    kv_type: str = "f16"  # K/V cache storage: "f16" or "q8_0" (rows quantised as they are written)
 
     @property
     def capacity(self) -> int:
@@ -83,6 +84,9 @@ WORKLOADS = {
                                                                 tied=False),
                                  batch=16, steps=32, prefill=8192),
 }
+# the same 16-sequence workload with a packed Q8_0 K/V cache (the same seeded rows, quantised when written)
+WORKLOADS["llama3_8b_q8_b16_kvq8"] = WORKLOADS["llama3_8b_q8_b16"].with_(name="llama3_8b_q8_b16_kvq8",
+                                                                         kv_type="q8_0")
 
 
 def workload(name: str) -> Workload:

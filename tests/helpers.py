@@ -20,9 +20,9 @@ def oracle_model(shape: synth.ModelShape, weights=None, cache_dequant=True) -> o
     return oracle.OracleModel(oracle_config(shape), weights, cache_dequant=cache_dequant)
 
 
-def oracle_cache(wl: synth.Workload, seqs=None) -> oracle.OracleCache:
+def oracle_cache(wl: synth.Workload, seqs=None, kv_type: str = "f16") -> oracle.OracleCache:
     cfg = oracle_config(wl.shape)
-    cache = oracle.OracleCache(cfg, wl.batch, wl.capacity)
+    cache = oracle.OracleCache(cfg, wl.batch, wl.capacity, kv_type=kv_type)
     for b in (range(wl.batch) if seqs is None else seqs):
         for l in range(wl.shape.n_layers):
             k, v = synth.kv_prefill(wl, b, l)
@@ -48,9 +48,9 @@ def gpu_model(shape, weights, max_batch=1):
     return runtime.DecodeModel(shape, weights, max_batch=max_batch)
 
 
-def gpu_state(model, wl, seqs=None):
+def gpu_state(model, wl, seqs=None, kv_type: str = "f16"):
     from block_quantized_token_gb300 import runtime
-    st = runtime.DecodeState(model, wl.batch, wl.capacity)
+    st = runtime.DecodeState(model, wl.batch, wl.capacity, kv_type=kv_type)
     for b in (range(wl.batch) if seqs is None else seqs):
         for l in range(wl.shape.n_layers):
             k, v = synth.kv_prefill(wl, b, l)
@@ -99,6 +99,30 @@ def top2_gap(logits):
 U32 = 2.0 ** -24  # unit roundoff of fp32
 
 
+def layer0_kv_exact(model, shape, token: int, pos: int):
+    """The layer-0 K row (after RoPE) and V row that `token` at `pos` appends, in float64, with the element-wise
+    bound on the GPU's fp32 values before any rounding to the cache type (layer0_kv_tolerance derives it).
+    Returns (k, v, delta_k, delta_v), each [n_kv_heads * hd]."""
+    s = shape
+    x = model.embedding_rows([token])[0]
+    g = model.gain("blk.0.attn_norm.weight")
+    K = s.dim
+    f = 1.0 / np.sqrt(np.mean(x * x) + s.rms_eps)
+    u = x * g
+
+    def pre(name):
+        w = model.matrix(name)
+        y = f * (w.astype(np.float64) @ u)
+        gb = (K // 32 + 9) * 2.0 ** -23 * (np.abs(w.astype(np.float64)) @ np.abs(u))
+        return y, f * gb + np.abs(y) * ((K / 64 + 15) * U32 + 2 * U32)
+
+    yk, dk = pre("blk.0.attn_k.weight")
+    yv, dv = pre("blk.0.attn_v.weight")
+    dpair = dk[0::2] + dk[1::2] + (np.abs(yk[0::2]) + np.abs(yk[1::2])) * 4 * U32
+    kr = oracle.rope(yk.reshape(s.n_kv_heads, s.head_dim), pos, s.rope_base).reshape(-1)
+    return kr, yv, np.repeat(dpair, 2), dv
+
+
 def layer0_kv_tolerance(model, shape, token: int, pos: int):
     """Element-wise bound on |GPU fp16 row - oracle fp16 row| for the K and V rows that layer 0 appends for
     `token` at `pos`, derived from the GPU's fp32 arithmetic.
@@ -115,28 +139,39 @@ def layer0_kv_tolerance(model, shape, token: int, pos: int):
     rotation's two products and one sum).  Two values within delta round to fp16 values at most
     delta + one fp16 ulp (at the larger magnitude) apart.  Returns (tol_k, tol_v), each [n_kv_heads * hd].
     """
-    s = shape
-    x = model.embedding_rows([token])[0]
-    g = model.gain("blk.0.attn_norm.weight")
-    K = s.dim
-    f = 1.0 / np.sqrt(np.mean(x * x) + s.rms_eps)
-    u = x * g
-
-    def pre(name):
-        w = model.matrix(name)
-        y = f * (w.astype(np.float64) @ u)
-        gb = (K // 32 + 9) * 2.0 ** -23 * (np.abs(w.astype(np.float64)) @ np.abs(u))
-        return y, f * gb + np.abs(y) * ((K / 64 + 15) * U32 + 2 * U32)
-
-    yk, dk = pre("blk.0.attn_k.weight")
-    yv, dv = pre("blk.0.attn_v.weight")
-    # rotation: the pair's two errors and the rotation's own rounding
-    dpair = dk[0::2] + dk[1::2] + (np.abs(yk[0::2]) + np.abs(yk[1::2])) * 4 * U32
-    dk_rot = np.repeat(dpair, 2)
-    kr = oracle.rope(yk.reshape(s.n_kv_heads, s.head_dim), pos, s.rope_base).reshape(-1)
+    kr, yv, dk_rot, dv = layer0_kv_exact(model, shape, token, pos)
 
     def tol(y, d):
         big = np.abs(y) + d
         return np.abs(np.spacing(big.astype(np.float16))).astype(np.float64) + d
 
     return tol(kr, dk_rot), tol(yv, dv)
+
+
+def check_q8_blocks(d_got, q_got, x, delta):
+    """GPU Q8_0 blocks (d [n/32] fp16, q [n] int8) of a row whose exact value is x (float64 [n]) and whose GPU
+    fp32 value before quantising lies within delta of it.  The codes are the quantiser's (float32, see
+    oracle.quantize_kv_q8_0) for some row within delta of x: d equals the oracle's d unless amax / 127 lies
+    within reach of an fp16 rounding boundary, and each q equals the oracle's code unless x / d lies within
+    reach of a half-integer, where it may be one off.  Returns the number of such one-off codes."""
+    x = np.asarray(x, np.float64)
+    d_ref, q_ref = oracle.quantize_kv_q8_0(x.astype(np.float32))
+    d_got = np.asarray(d_got, np.float16).reshape(d_ref.shape)
+    q_got = np.asarray(q_got, np.int8).reshape(q_ref.shape)
+    delta = 2.0 * np.asarray(delta, np.float64) + 2.0 ** -22 * np.abs(x)  # margin for the float32 steps
+    xb, db = x.reshape(-1, 32), delta.reshape(-1, 32)
+    amax, amax_d = np.abs(xb).max(axis=1), db.max(axis=1)
+    d_lo = ((amax - amax_d) / 127).astype(np.float32).astype(np.float16)
+    d_hi = ((amax + amax_d) / 127).astype(np.float32).astype(np.float16)
+    d_diff = d_got.reshape(-1) != d_ref.reshape(-1)
+    assert not (d_diff & (d_lo == d_hi)).any(), "a block scale differs where no rounding boundary is near"
+    assert (d_got.reshape(-1) >= d_lo).all() and (d_got.reshape(-1) <= d_hi).all(), "a block scale out of reach"
+    same = ~d_diff
+    qg, qr = q_got.reshape(-1, 32)[same].astype(np.int64), q_ref.reshape(-1, 32)[same].astype(np.int64)
+    dd = d_ref.reshape(-1)[same].astype(np.float64)[:, None]
+    r, rd = xb[same] / np.where(dd > 0, dd, 1), db[same] / np.where(dd > 0, dd, 1)
+    frac = np.abs(np.abs(r) - np.floor(np.abs(r)) - 0.5)  # distance of |x / d| from a half-integer
+    off = qg != qr
+    assert (np.abs(qg - qr) <= 1).all(), "a code more than one step from the oracle's"
+    assert not (off & (frac > rd)).any(), "a code differs where x / d is not near a half-integer"
+    return int(off.sum())

@@ -88,3 +88,10 @@ def test_null_arguments_rejected(er):
     with pytest.raises(er.ErError) as e:
         er.er_kv_set_wide_gemv(0, er.ER_WIDE_TCGEN05)
     assert e.value.status == er.ER_EINVAL
+    with pytest.raises(er.ErError) as e:
+        er.er_kv_create_typed(0, 1, 16, er.ER_Q8_0)
+    assert e.value.status == er.ER_EINVAL
+    with pytest.raises(er.ErError) as e:
+        er.er_kv_read_blocks(0, 0, 0, 0, 1, 0, 0, 0)
+    assert e.value.status == er.ER_EINVAL
+    assert er.er_kv_type(None) == -1
