@@ -509,6 +509,64 @@ def gemv_sweep(reps: int = 50) -> dict:
     return out
 
 
+def run_prefill(args) -> dict:
+    """Chunked prefill of `args.prefill` seeded tokens into one sequence of the workload's model (a fresh
+    cache from position 0), timed with CUDA events over `args.steps` repetitions after `args.warmup`."""
+    import torch
+
+    from block_quantized_token_gb300 import build as libbuild
+    if not libbuild.up_to_date():
+        libbuild.build()
+    from block_quantized_token_gb300 import runtime
+    wl = synth.workload(args.workload)
+    s = wl.shape
+    n = args.prefill
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    threads = min(32, os.cpu_count() or 1)
+    model = runtime.DecodeModel(s, synth.model_weights(s, threads=threads), max_batch=1)
+    state = runtime.DecodeState(model, 1, n, kv_type=wl.kv_type)
+    toks = torch.tensor(np.random.default_rng(1).integers(0, s.vocab, n).astype(np.int32), device=dev)
+    logits = torch.empty(s.vocab, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    for _ in range(args.warmup):
+        state.prefill(0, toks, 0, logits, stream=stream.cuda_stream)
+    stream.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            state.prefill(0, toks, 0, logits, stream=stream.cuda_stream)
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    if state.device_error()[1]:
+        raise RuntimeError("device error flags after prefill")
+    # algorithmic bytes: every chunk of 16 reads the layers' weights once and the K/V rows below its last
+    # position once, and writes its rows; the head once for the last token
+    w = matrix_bytes(s)
+    per_layer_w = w["qkv"] + w["wo"] + w["gateup"] + w["down"]
+    kv_row = s.kvd / 32 * 34 if wl.kv_type == "q8_0" else s.kvd * 2
+    chunks = (n + 15) // 16
+    rows_read = sum(min(n, 16 * (c + 1)) for c in range(chunks))
+    nbytes = chunks * s.n_layers * per_layer_w + w["head"] + s.n_layers * 2 * kv_row * (rows_read + n)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    state.close()
+    model.close()
+    return {"metric": "prefill tok/s (chunks of 16 tokens through the batched decode kernels)", "value": n / (ms / 1e3),
+            "unit": "tok/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_prefill": ms,
+            "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "prompt_tokens": n, "kv_cache": wl.kv_type, "chunk": 16},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+                         "bytes_per_prefill": nbytes},
+            "clocks": clock_info}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -526,6 +584,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the layer count (smaller cases for profiling; not a bench workload)")
+    ap.add_argument("--prefill", type=int, default=None,
+                    help="time er_prefill of this many tokens into one sequence of the workload's model instead")
     args = ap.parse_args()
 
     if args.gemv_sweep:
@@ -562,6 +622,10 @@ def main():
         print(json.dumps(line))
         return
 
+    if args.prefill:
+        if rank == 0:
+            print(json.dumps(run_prefill(args)))
+        return
     if world > 1:
         import torch
         import torch.distributed as dist

@@ -254,12 +254,11 @@ er_status er_kv_create(er_model *m, int32_t batch, int32_t capacity, er_kv **out
     return er_kv_create_typed(m, batch, capacity, ER_F16, out);
 }
 
-er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32_t kv_type, er_kv **out) {
-    if (!m || !out) return fail(ER_EINVAL, "NULL argument");
+// A decode state; with `owner`, a 16-column prefill view of the owner's cache: it allocates its own
+// activations and scratch but takes the owner's cache and flag word.
+static er_status kv_create(er_model *m, int32_t batch, int32_t capacity, int32_t kv_type, er_kv *owner,
+                           er_kv **out) {
     const er_config &c = m->cfg;
-    if (batch < 1 || batch > c.max_batch) return fail(ER_EINVAL, "batch must be in 1..max_batch");
-    if (capacity < 1 || capacity > (1 << 24)) return fail(ER_EINVAL, "capacity out of range");
-    if (kv_type != ER_F16 && kv_type != ER_Q8_0) return fail(ER_EINVAL, "kv_type must be ER_F16 or ER_Q8_0");
     er_kv *kv = new er_kv();
     kv->m = m;
     kv->B = batch;
@@ -268,6 +267,11 @@ er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32
     kv->kc = kv->vc = nullptr;
     kv->kvq = {};
     kv->kstage = kv->vstage = nullptr;
+    kv->seqmap = nullptr;
+    kv->pf = nullptr;
+    kv->view = owner != nullptr;
+    kv->pf_pos = kv->pf_seq = nullptr;
+    kv->pf_logits = nullptr;
     kv->cap_stream = nullptr;
     kv->graph_calls = 0;
     kv->bar_extra = 0;
@@ -288,7 +292,15 @@ er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32
         e = dalloc(kv->allocs, p, bytes);
         if (e == cudaSuccess && zero) e = cudaMemset(*p, 0, bytes);
     };
-    if (kv_type == ER_F16) {
+    if (owner) {
+        kv->kc = owner->kc;
+        kv->vc = owner->vc;
+        kv->kvq = owner->kvq;
+        A(&kv->pf_pos, 16 * sizeof(int32_t));
+        A(&kv->pf_seq, 16 * sizeof(int32_t));
+        A(&kv->pf_logits, (size_t)16 * c.vocab * sizeof(float), false);
+        kv->seqmap = kv->pf_seq;
+    } else if (kv_type == ER_F16) {
         A(&kv->kc, cache_elems * sizeof(__half));
         A(&kv->vc, cache_elems * sizeof(__half));
     } else {
@@ -299,6 +311,8 @@ er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32
         kv->kvq.L = c.n_layers;
         kv->kvq.KV = c.n_kv_heads;
         kv->kvq.cap = capacity;
+    }
+    if (kv_type == ER_Q8_0) {
         A(&kv->kstage, (size_t)batch * kvd * sizeof(float));
         A(&kv->vstage, (size_t)batch * kvd * sizeof(float));
     }
@@ -335,7 +349,10 @@ er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32
     }
     A(&kv->amax, 16 * sizeof(unsigned long long));
     A(&kv->done, sizeof(int));
-    A(&kv->flags, sizeof(int));
+    if (owner)
+        kv->flags = owner->flags;  // prefill errors show in the owner's er_get_device_error
+    else
+        A(&kv->flags, sizeof(int));
     if (e == cudaSuccess) {
         // RoPE table: angle p * base^(-2i/hd) in double, cos/sin rounded to fp32
         std::vector<float2> cs((size_t)capacity * (hd / 2));
@@ -356,7 +373,7 @@ er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32
             R[i] = mats[i]->R;
             UPR[i] = mats[i]->UPR;
         }
-        kv->step_ok = e == cudaSuccess && kv_type == ER_F16 &&
+        kv->step_ok = e == cudaSuccess && kv_type == ER_F16 && !owner &&
                       step_supported(c.w_type, hd, G, batch, c.n_kv_heads, capacity, max_k, R, UPR, m->num_sms);
         kv->schedule = kv->step_ok ? ER_SCHEDULE_PERSISTENT : ER_SCHEDULE_KERNELS;
         A(&kv->step_layers, (size_t)c.n_layers * sizeof(StepLayer), false);
@@ -389,8 +406,18 @@ er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32
     return ER_OK;
 }
 
+er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity, int32_t kv_type, er_kv **out) {
+    if (!m || !out) return fail(ER_EINVAL, "NULL argument");
+    const er_config &c = m->cfg;
+    if (batch < 1 || batch > c.max_batch) return fail(ER_EINVAL, "batch must be in 1..max_batch");
+    if (capacity < 1 || capacity > (1 << 24)) return fail(ER_EINVAL, "capacity out of range");
+    if (kv_type != ER_F16 && kv_type != ER_Q8_0) return fail(ER_EINVAL, "kv_type must be ER_F16 or ER_Q8_0");
+    return kv_create(m, batch, capacity, kv_type, nullptr, out);
+}
+
 void er_kv_destroy(er_kv *kv) {
     if (!kv) return;
+    er_kv_destroy(kv->pf);
     for (auto &g : kv->graphs) cudaGraphExecDestroy(g.exec);
     if (kv->cap_stream) cudaStreamDestroy(kv->cap_stream);
     free_all(kv->allocs);
@@ -541,9 +568,11 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
             a.cap = kv->cap;
             a.k_stage = kv->kstage;  // Q8_0 cache: fp32 rows, quantised by the next launch
             a.v_stage = kv->vstage;
+            a.seqmap = kv->seqmap;
             cudaError_t e = gemv_all(kv, EPI_QKV, a, st, pdl);
             if (e == cudaSuccess && kv->kv_type == ER_Q8_0)
-                e = launch_kvq_stage(kv->kstage, kv->vstage, positions, kv->B, kv->kvq, c.head_dim, l, st, pdl);
+                e = launch_kvq_stage(kv->kstage, kv->vstage, positions, kv->seqmap, kv->B, kv->kvq, c.head_dim, l,
+                                     st, pdl);
             return e;
         }
         case ER_STAGE_ATTN: {
@@ -555,6 +584,7 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
             a.vq = kv->kvq.vq;
             a.kd = kv->kvq.kd;
             a.vd = kv->kvq.vd;
+            a.seqmap = kv->seqmap;
             a.positions = positions;
             a.o = kv->o;
             a.part = kv->attn_part;
@@ -726,6 +756,44 @@ er_status er_launch_stage(er_kv *kv, int32_t stage, int32_t layer, const int32_t
     if (stage < ER_STAGE_EMBED || stage > ER_STAGE_HEAD) return fail(ER_EINVAL, "bad stage");
     if (layer < 0 || layer >= kv->m->cfg.n_layers) return fail(ER_EINVAL, "layer out of range");
     ER_CUDA(enqueue_stage(kv, stage, layer, tokens, positions, logits, argmax, (cudaStream_t)stream, false));
+    return ER_OK;
+}
+
+er_status er_prefill(er_kv *kv, int32_t seq, const int32_t *tokens, int32_t n, int32_t start, float *logits,
+                     void *stream) {
+    if (!kv) return fail(ER_EINVAL, "kv is NULL");
+    if (kv->view) return fail(ER_EINVAL, "not a decode state");
+    if (seq < 0 || seq >= kv->B) return fail(ER_EINVAL, "seq out of range");
+    if (n < 0 || start < 0 || (long long)start + n > kv->cap) return fail(ER_EINVAL, "positions out of range");
+    if (n == 0) return ER_OK;
+    if (!tokens) return fail(ER_EINVAL, "tokens is NULL");
+    if (!kv->pf) {
+        er_kv *v = nullptr;
+        er_status s = kv_create(kv->m, 16, kv->cap, kv->kv_type, kv, &v);
+        if (s != ER_OK) return s;
+        kv->pf = v;
+    }
+    er_kv *v = kv->pf;
+    v->wide_variant = kv->wide_variant;
+    const cudaStream_t st = (cudaStream_t)stream;
+    const int L = kv->m->cfg.n_layers, V = kv->m->cfg.vocab;
+    for (int c0 = 0; c0 < n; c0 += 16) {
+        const int cols = n - c0 < 16 ? n - c0 : 16;
+        const bool last = c0 + cols == n;
+        v->B = cols;
+        ER_CUDA(launch_prefill_setup(v->pf_pos, v->pf_seq, start + c0, seq, cols, st));
+        cudaError_t e = enqueue_stage(v, ER_STAGE_EMBED, 0, tokens + c0, v->pf_pos, nullptr, nullptr, st, true);
+        for (int l = 0; l < L && e == cudaSuccess; ++l)
+            for (int sg = ER_STAGE_QKV; sg <= ER_STAGE_DOWN && e == cudaSuccess; ++sg)
+                e = enqueue_stage(v, sg, l, tokens + c0, v->pf_pos, nullptr, nullptr, st, true);
+        if (e == cudaSuccess && last && logits) {
+            e = enqueue_stage(v, ER_STAGE_HEAD, 0, tokens + c0, v->pf_pos, v->pf_logits, nullptr, st, true);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(logits, v->pf_logits + (size_t)(cols - 1) * V, (size_t)V * sizeof(float),
+                                    cudaMemcpyDeviceToDevice, st);
+        }
+        ER_CUDA(e);
+    }
     return ER_OK;
 }
 

@@ -186,6 +186,7 @@ __device__ inline void gv_epilogue(const GemvArgs &a, int rg, float v0, float v1
         v1 *= f;
         const int pos = a.pos_s ? a.pos_s[bt] : a.positions[bt];
         if (pos < 0 || pos >= a.cap) return;
+        const int sq = a.seqmap ? a.seqmap[bt] : bt;  // the column's sequence in the cache
         int r0 = 16 * rg + 2 * g;  // RoPE pair (r0, r0 + 1)
         if (r0 >= a.qd + 2 * a.kvd) return;
         if (r0 < a.qd + a.kvd) {  // q or k: rotate
@@ -202,7 +203,7 @@ __device__ inline void gv_epilogue(const GemvArgs &a, int rg, float v0, float v1
                     *reinterpret_cast<float2 *>(a.k_stage + (size_t)bt * a.kvd + base) = make_float2(o0, o1);
                 } else {
                     int kvh = base / a.hd;
-                    size_t off = ((((size_t)bt * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
+                    size_t off = ((((size_t)sq * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
                     *reinterpret_cast<__half2 *>(a.kc + off) = __floats2half2_rn(o0, o1);
                 }
             }
@@ -212,7 +213,7 @@ __device__ inline void gv_epilogue(const GemvArgs &a, int rg, float v0, float v1
                 *reinterpret_cast<float2 *>(a.v_stage + (size_t)bt * a.kvd + base) = make_float2(v0, v1);
             } else {
                 int kvh = base / a.hd, dd = base % a.hd;
-                size_t off = ((((size_t)bt * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
+                size_t off = ((((size_t)sq * a.L + a.layer) * a.KV + kvh) * a.cap + pos) * a.hd + dd;
                 *reinterpret_cast<__half2 *>(a.vc + off) = __floats2half2_rn(v0, v1);
             }
         }

@@ -55,6 +55,7 @@ struct GemvArgs {
     float *q_out;
     __half *kc, *vc;
     float *k_stage, *v_stage;  // non-null: K/V rows go to fp32 staging [batch][kvd] instead of kc / vc
+    const int32_t *seqmap;     // cache sequence of each column (nullptr: column b is sequence b)
     const float2 *rope;
     const int32_t *positions;
     int qd, kvd, hd, KV, L, layer, cap;
@@ -108,6 +109,7 @@ struct AttnArgs {
     const __half *kc, *vc;        // fp16 cache [B][L][KV][cap][hd], or
     const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): values [B][L][KV][cap][hd]
     const __half *kd, *vd;        //   and block scales [B][L][KV][cap][hd / 32]
+    const int32_t *seqmap;        // cache sequence of each column (nullptr: column b is sequence b)
     const int32_t *positions;
     float *o;  // [B][qd]
     float *part;  // warp states of pairs shared by warps (attention_part_floats)
@@ -131,8 +133,9 @@ struct KvqCache {
 cudaError_t launch_kvq_write(const __half *k_rows, const __half *v_rows, int n, const KvqCache &c, int hd, int seq,
                              int layer, int start, cudaStream_t st);
 // the step's fp32 staging rows [B][KV * hd] -> cache row positions[b] of `layer`
-cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const int32_t *positions, int B,
-                             const KvqCache &c, int hd, int layer, cudaStream_t st, bool pdl);
+cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const int32_t *positions,
+                             const int32_t *seqmap, int B, const KvqCache &c, int hd, int layer, cudaStream_t st,
+                             bool pdl);
 // cache rows start.. of (seq, layer) -> GGUF Q8_0 blocks [n][KV * hd / 32][34] (device)
 cudaError_t launch_kvq_read(uint8_t *k_out, uint8_t *v_out, int n, const KvqCache &c, int hd, int seq, int layer,
                             int start, cudaStream_t st);
@@ -194,6 +197,8 @@ struct EmbedArgs {
 };
 cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_positions_increment(int32_t *pos, int n, cudaStream_t st);
+// prefill chunk columns: pos[i] = start + i, seq[i] = s for i < n
+cudaError_t launch_prefill_setup(int32_t *pos, int32_t *seq, int start, int s, int n, cudaStream_t st);
 
 // one device allocation outside any owner list, counted and failure-injectable like the library's own
 cudaError_t device_alloc(void **p, size_t bytes);
@@ -264,6 +269,12 @@ struct er_kv {
     __half *kc, *vc;             // fp16 cache (ER_KV_F16)
     er::KvqCache kvq;            // Q8_0 cache (ER_KV_Q8_0)
     float *kstage, *vstage;      // Q8_0: the step's new K/V rows in fp32 [B][kvd]
+    const int32_t *seqmap;       // cache sequence of each column (nullptr: column b is sequence b)
+    // chunked prefill: a 16-column view sharing this state's cache (created by the first er_prefill)
+    er_kv *pf;
+    bool view;                   // this state is such a view: cache and flags belong to its owner
+    int32_t *pf_pos, *pf_seq;    // view: positions and sequences of the chunk's columns [16]
+    float *pf_logits;            // view: logits of the chunk's columns [16][vocab]
     float2 *rope;
     float *x, *q, *o, *a;
     float *attn_part;

@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArg
         const int r0 = u - seg_start, r1 = (wb < seg_end ? wb : seg_end) - seg_start;
         const bool first_piece = u == wa;
         u = wb < seg_end ? wb : seg_end;
-        const size_t head = ((size_t)b * a.L + a.layer) * a.KV + kvh;
+        const size_t head = ((size_t)(a.seqmap ? a.seqmap[b] : b) * a.L + a.layer) * a.KV + kvh;
         TaSrc src;
         if constexpr (Q8) {
             src.K = src.V = nullptr;

@@ -67,11 +67,11 @@ __global__ void kvq_write_kernel(const __half *k_rows, const __half *v_rows, int
 }
 
 // The step's new rows: fp32 staging [B][KV * hd] (written by the Q/K/V epilogue) -> cache row
-// positions[b] of layer `layer`, for every sequence whose position is in range; one warp per
-// (sequence, head, K or V).
+// positions[b] of sequence seqmap[b] (b without a map) of layer `layer`, for every column whose
+// position is in range; one warp per (column, head, K or V).
 template <int E>
-__global__ void kvq_stage_kernel(const float *k_stage, const float *v_stage, const int32_t *positions, int B,
-                                 KvqCache c, int layer) {
+__global__ void kvq_stage_kernel(const float *k_stage, const float *v_stage, const int32_t *positions,
+                                 const int32_t *seqmap, int B, KvqCache c, int layer) {
     pdl_wait();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
@@ -85,7 +85,7 @@ __global__ void kvq_stage_kernel(const float *k_stage, const float *v_stage, con
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] = __ldcg(src + e);
-    const size_t r = kvq_head(b, c.L, layer, c.KV, h) * c.cap + pos;
+    const size_t r = kvq_head(seqmap ? seqmap[b] : b, c.L, layer, c.KV, h) * c.cap + pos;
     kvq_row<E>(x, (kv ? c.vq : c.kq) + r * hd, (kv ? c.vd : c.kd) + r * (hd / 32), lane);
 }
 
@@ -124,8 +124,9 @@ cudaError_t launch_kvq_write(const __half *k_rows, const __half *v_rows, int n, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const int32_t *positions, int B,
-                             const KvqCache &c, int hd, int layer, cudaStream_t st, bool pdl) {
+cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const int32_t *positions,
+                             const int32_t *seqmap, int B, const KvqCache &c, int hd, int layer, cudaStream_t st,
+                             bool pdl) {
     const int warps = 2 * B * c.KV, per = 8;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -136,8 +137,10 @@ cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const i
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (hd == 128) return cudaLaunchKernelEx(&cfg, kvq_stage_kernel<4>, k_stage, v_stage, positions, B, c, layer);
-    if (hd == 64) return cudaLaunchKernelEx(&cfg, kvq_stage_kernel<2>, k_stage, v_stage, positions, B, c, layer);
+    if (hd == 128)
+        return cudaLaunchKernelEx(&cfg, kvq_stage_kernel<4>, k_stage, v_stage, positions, seqmap, B, c, layer);
+    if (hd == 64)
+        return cudaLaunchKernelEx(&cfg, kvq_stage_kernel<2>, k_stage, v_stage, positions, seqmap, B, c, layer);
     return cudaErrorInvalidValue;
 }
 

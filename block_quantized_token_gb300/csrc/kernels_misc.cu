@@ -151,4 +151,17 @@ cudaError_t launch_positions_increment(int32_t *pos, int n, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+__global__ void prefill_setup_kernel(int32_t *pos, int32_t *seq, int start, int s, int n) {
+    const int i = threadIdx.x;
+    if (i < n) {
+        pos[i] = start + i;
+        seq[i] = s;
+    }
+}
+
+cudaError_t launch_prefill_setup(int32_t *pos, int32_t *seq, int start, int s, int n, cudaStream_t st) {
+    prefill_setup_kernel<<<1, 32, 0, st>>>(pos, seq, start, s, n);
+    return cudaGetLastError();
+}
+
 }  // namespace er

@@ -60,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "er_kv_create_typed": (I32, [VP, I32, I32, I32, P(VP)]),
         "er_kv_type": (I32, [VP]),
         "er_kv_read_blocks": (I32, [VP, I32, I32, I32, I32, VP, VP, VP]),
+        "er_prefill": (I32, [VP, I32, VP, I32, I32, VP, VP]),
         "er_kv_destroy": (None, [VP]),
         "er_kv_layer_ptrs": (I32, [VP, I32, I32, P(VP), P(VP)]),
         "er_kv_write": (I32, [VP, I32, I32, I32, I32, VP, VP, VP]),
@@ -111,7 +112,7 @@ EXPORTED = ("er_model_create", "er_model_destroy", "er_model_device_bytes", "er_
             "er_kv_launches_per_step", "er_kv_cached_graphs", "er_kv_inject_wait_shortfall", "er_set_wait_limit_ns",
             "er_debug_fail_allocation", "er_debug_live_allocations", "er_gguf_open", "er_gguf_close",
             "er_gguf_tensor_count", "er_gguf_tensor_info", "er_gguf_find", "er_gguf_config",
-            "er_model_create_from_gguf", "er_kv_create_typed", "er_kv_type", "er_kv_read_blocks", "er_status_str",
+            "er_model_create_from_gguf", "er_kv_create_typed", "er_kv_type", "er_kv_read_blocks", "er_prefill", "er_status_str",
             "er_last_error")
 
 
@@ -166,6 +167,11 @@ def er_kv_type(kv: int | None) -> int:
 def er_kv_read_blocks(kv: int, seq: int, layer: int, start: int, n: int, k_blocks: int, v_blocks: int,
                       stream: int = 0) -> None:
     _check(_lib.er_kv_read_blocks(kv, seq, layer, start, n, k_blocks, v_blocks, stream), "er_kv_read_blocks")
+
+
+def er_prefill(kv: int, seq: int, tokens: int | None, n: int, start: int, logits: int | None,
+               stream: int = 0) -> None:
+    _check(_lib.er_prefill(kv, seq, tokens, n, start, logits, stream), "er_prefill")
 
 
 def er_kv_destroy(kv: int) -> None:

@@ -125,6 +125,13 @@ class DecodeState:
             out += [d, q]
         return tuple(out)
 
+    def prefill(self, seq: int, tokens: torch.Tensor, start: int, logits: torch.Tensor | None = None,
+                stream: int | None = None) -> None:
+        """Run the decoder over device int32 `tokens` of sequence `seq` at positions start.., writing the cache."""
+        st = torch.cuda.current_stream(self.model.device).cuda_stream if stream is None else stream
+        er.er_prefill(self.handle, seq, tokens.data_ptr() if tokens.numel() else None, int(tokens.numel()), start,
+                      None if logits is None else logits.data_ptr(), st)
+
     def step(self, tokens: torch.Tensor, positions: torch.Tensor, logits: torch.Tensor | None,
              argmax: torch.Tensor | None, graph: bool = True, stream: int | None = None) -> None:
         st = torch.cuda.current_stream(self.model.device).cuda_stream if stream is None else stream

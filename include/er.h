@@ -134,6 +134,25 @@ ER_API er_status er_kv_create_typed(er_model *m, int32_t batch, int32_t capacity
 /* The cache storage of kv (ER_F16 or ER_Q8_0), or -1 for NULL. */
 ER_API int32_t er_kv_type(const er_kv *kv);
 
+/* Chunked prefill ("EdgeRunner Core Architecture" section 9.1, the fused
+ * prefill pass; "alpaca.swift" Results, prefill): runs the decoder over the n
+ * tokens tokens_dev[0..n-1] (device int32) of sequence `seq` at positions
+ * start..start+n-1, writing their K/V rows of every layer into the cache, in
+ * chunks of 16 tokens.  A chunk is one pass of the step's kernels over 16
+ * columns that all belong to sequence `seq`: each GEMV reads its weights once
+ * for the chunk, and the token at position p attends rows 0..p (the chunk's
+ * earlier rows included), so the result equals n decode steps.  Rows below
+ * `start` must already hold that sequence's keys and values; other sequences
+ * are untouched.  logits_dev (fp32 [vocab], may be NULL) receives the logits of
+ * the last token.  Queued on `stream`, no synchronisation.  The first call
+ * allocates a 16-column scratch (activations and partials, about as much as a
+ * 16-sequence decode state without its cache) and synchronises the device; it is
+ * freed with kv.  Bad tokens and positions set the flags er_get_device_error
+ * reports.  ER_EINVAL: kv NULL, seq out of range, start < 0, n < 0,
+ * start + n > capacity, or tokens_dev NULL with n > 0. */
+ER_API er_status er_prefill(er_kv *kv, int32_t seq, const int32_t *tokens_dev, int32_t n, int32_t start,
+                            float *logits_dev, void *stream);
+
 /* Reads cache rows start..start+n-1 of sequence `seq`, layer `layer` of an
  * ER_Q8_0 cache as GGUF Q8_0 blocks: k_blocks_dev / v_blocks_dev receive
  * [n][n_kv_heads * head_dim / 32] blocks of 34 bytes (little-endian fp16 d,
