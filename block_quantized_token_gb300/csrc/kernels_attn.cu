@@ -248,23 +248,23 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
             }
         } else {
             const uint32_t qslot = ring_s + (uint32_t)((k % NS) * Q::SLOT);
-            // the quantised K and V tiles into fp16 (exact), in the fp16 path's swizzled layout
+            // the quantised K and V tiles into fp16 (exact), in the fp16 path's swizzled layout: each lane
+            // takes 8 codes (one fp16 chunk), so that the 8 lanes of each store phase fill 8 distinct chunks
 #pragma unroll
             for (int kv = 0; kv < 2; ++kv)
 #pragma unroll
-                for (int i = 0; i < Q::QT / 16 / 32; ++i) {
-                    const int ci = lane + 32 * i, row = ci / (HD / 16), col = ci % (HD / 16);
-                    const uint4 w = lds128(qslot + kv * (Q::QT + Q::ST) + ci * 16);
-                    uint32_t h[8];
-                    q8_word_to_h2(w.x ^ 0x80808080u, h[0], h[1]);
-                    q8_word_to_h2(w.y ^ 0x80808080u, h[2], h[3]);
-                    q8_word_to_h2(w.z ^ 0x80808080u, h[4], h[5]);
-                    q8_word_to_h2(w.w ^ 0x80808080u, h[6], h[7]);
-                    const uint32_t base = conv + kv * C::TILEB + row * C::ROWB;
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + (((2 * col) ^ (row & 7)) << 4)),
-                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3]) : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + (((2 * col + 1) ^ (row & 7)) << 4)),
-                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7]) : "memory");
+                for (int i = 0; i < Q::QT / 8 / 32; ++i) {
+                    const int ci = lane + 32 * i, row = ci / (HD / 8), col = ci % (HD / 8);
+                    uint32_t w0, w1;
+                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                                 : "=r"(w0), "=r"(w1)
+                                 : "r"(qslot + kv * (Q::QT + Q::ST) + ci * 8));
+                    uint32_t h[4];
+                    q8_word_to_h2(w0 ^ 0x80808080u, h[0], h[1]);
+                    q8_word_to_h2(w1 ^ 0x80808080u, h[2], h[3]);
+                    const uint32_t dst = conv + kv * C::TILEB + row * C::ROWB + ((col ^ (row & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[0]), "r"(h[1]), "r"(h[2]),
+                                 "r"(h[3]) : "memory");
                 }
             const int rows4[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
