@@ -102,6 +102,10 @@ STEP_KERNEL_SOURCES = KERNEL_SOURCES["step_kernel"]
 KERNEL_TRAFFIC = {
     # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --workload smollm_q8 --steps 4 --warmup 3 --no-cpu-baseline`
     ("smollm_q8", "step_kernel"): ("35d7ab1969b026e2", 190641152 + 3227648),
+    # attn_tc_kernel<128, 4, fp16 / Q8_0 cache>, 4th launch of `bench.py [--workload llama3_8b_q8_b16_kvq8]
+    # --layers 1 --steps 1 --warmup 3 --no-cpu-baseline` (one layer: the per-layer shape of the full model)
+    ("llama3_8b_q8_b16", "attn"): ("38052aa7bf3d8f34", 537800704 + 9338368),
+    ("llama3_8b_q8_b16_kvq8", "attn"): ("38052aa7bf3d8f34", 286342400 + 9010688),
 }
 
 
@@ -353,7 +357,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                        "step_bytes": bytes_step, "step_gbs": bytes_step / (ms / K / 1e3) / 1e9,
                        "step_roofline_frac": bytes_step / (ms / K / 1e3) / 1e9 / measured_peaks()["hbm_gbs"],
                        "step_frac_of_8tbs": bytes_step / (ms / K / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                       "l2": ("L2 flushed between steps (256 MiB write), step graphs timed alone" if args.flush_l2
+                       "l2": ("L2 flushed between steps (a 256 MiB read), step graphs timed alone" if args.flush_l2
                               else "inputs larger than L2" if bytes_step > 129e6
                               else "L2-resident working set, not flushed"),
                        "parallelism": f"replicas x{world}", "setup_s": round(setup_s, 1)},

@@ -36,3 +36,23 @@ def test_step_bytes_grow_with_cached_rows():
     s = wl.shape
     diff = bench.step_bytes(wl, pos + 1) - bench.step_bytes(wl, pos)
     assert diff == s.n_layers * wl.batch * s.kvd * 2 * 2
+
+
+def test_q8_cache_bytes():
+    """With a Q8_0 cache a cached row costs kvd/32 blocks of 34 bytes per side, read once by attention."""
+    wl = synth.workload("tiny").with_(batch=2, kv_type="q8_0")
+    s = wl.shape
+    pos = np.array([4, 11])
+    diff = bench.step_bytes(wl, pos + 1) - bench.step_bytes(wl, pos)
+    assert diff == s.n_layers * wl.batch * (s.kvd // 32) * 34 * 2
+    # the new rows: fp32 staging written and read, then their blocks written, per side
+    f16 = bench.stage_bytes(wl.with_(kv_type="f16"), pos)["qkv"]
+    q8 = bench.stage_bytes(wl, pos)["qkv"]
+    assert q8 - f16 == wl.batch * 2 * (s.kvd * 4 * 2 + s.kvd / 32 * 34 - s.kvd * 2)
+
+
+def test_q8_cache_workload_is_the_8b_batch_with_a_q8_cache():
+    a, b = synth.workload("llama3_8b_q8_b16"), synth.workload("llama3_8b_q8_b16_kvq8")
+    assert b.kv_type == "q8_0" and a.kv_type == "f16"
+    assert (a.shape, a.batch, a.steps, a.prefill) == (b.shape, b.batch, b.steps, b.prefill)
+    assert np.array_equal(synth.kv_prefill(a.with_(shape=TINY), 1, 0)[0], synth.kv_prefill(b.with_(shape=TINY), 1, 0)[0])
