@@ -25,7 +25,8 @@
 namespace er {
 
 constexpr int GW_WARPS = 16;
-constexpr int GW_SLOTS = 3;                   // ring slots per warp
+constexpr int GW_SLOTS = 2;                   // ring slots per warp
+constexpr int GW_SU = 4;                      // units per ring slot (one slot in flight while one is consumed)
 constexpr int GW_SLICE_UNITS = 16;            // 1024 columns
 constexpr int GW_NT = 4;                      // n8 tiles: 16 batch columns x (hi, lo)
 constexpr int GW_BLOCK_BYTES = GW_NT * 8 * 64;  // operand bytes of one 32-element block
@@ -35,7 +36,13 @@ static_assert(GW_WARPS * GW_SLOTS * 8 <= GW_OFF_RING, "mbarriers overlap the rin
 __host__ __device__ inline int gw_slices(int UPR) { return (UPR + GW_SLICE_UNITS - 1) / GW_SLICE_UNITS; }
 
 template <int QT>
-constexpr int gw_off_operand() { return GW_OFF_RING + GW_WARPS * GW_SLOTS * GvCfg<QT>::SLOT; }
+struct GwCfg {
+    static constexpr int UB = GvCfg<QT>::UB;
+    static constexpr int SU = GW_SU;
+    static constexpr int SLOT = GW_SU * UB;  // 4352 / 2304 bytes
+};
+template <int QT>
+constexpr int gw_off_operand() { return GW_OFF_RING + GW_WARPS * GW_SLOTS * GwCfg<QT>::SLOT; }
 template <int QT>
 constexpr int gw_smem() {
     // operand of 32 blocks, then per-column factors [16], per-(warp, segment) maxima [16][8], per-item sums of
@@ -140,7 +147,7 @@ __device__ inline void gw_logits(const GemvArgs &a, int rg, const float (&v)[GW_
 
 template <int QT, int EPI>
 __global__ void __launch_bounds__(GW_WARPS * 32, 1) gemv_wide_kernel(const GemvArgs a, float *wpart, float *wssq) {
-    using C = GvCfg<QT>;
+    using C = GwCfg<QT>;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     uint8_t *op = smem + gw_off_operand<QT>();
