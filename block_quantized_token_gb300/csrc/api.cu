@@ -304,13 +304,16 @@ static er_status kv_create(er_model *m, int32_t batch, int32_t capacity, int32_t
         A(&kv->kc, cache_elems * sizeof(__half));
         A(&kv->vc, cache_elems * sizeof(__half));
     } else {
-        A(&kv->kvq.kq, cache_elems);
-        A(&kv->kvq.vq, cache_elems);
-        A(&kv->kvq.kd, cache_elems / 32 * sizeof(__half));
-        A(&kv->kvq.vd, cache_elems / 32 * sizeof(__half));
+        const int rows = (capacity + 15) & ~15;  // whole tiles of 16 rows per head
+        const size_t q_elems = cache_elems / capacity * rows;
+        A(&kv->kvq.kq, q_elems);
+        A(&kv->kvq.vq, q_elems);
+        A(&kv->kvq.kd, q_elems / 32 * sizeof(__half));
+        A(&kv->kvq.vd, q_elems / 32 * sizeof(__half));
         kv->kvq.L = c.n_layers;
         kv->kvq.KV = c.n_kv_heads;
         kv->kvq.cap = capacity;
+        kv->kvq.rows = rows;
     }
     if (kv_type == ER_Q8_0) {
         A(&kv->kstage, (size_t)batch * kvd * sizeof(float));

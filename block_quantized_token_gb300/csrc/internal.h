@@ -107,8 +107,8 @@ int gemv_max_cols(int qt, int K);  // largest B <= 4 that gemv_fits
 struct AttnArgs {
     const float *q;  // [B][qd]
     const __half *kc, *vc;        // fp16 cache [B][L][KV][cap][hd], or
-    const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): values [B][L][KV][cap][hd]
-    const __half *kd, *vd;        //   and block scales [B][L][KV][cap][hd / 32]
+    const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): codes [B][L][KV][rows * hd] (kernels_kvq.cu order)
+    const __half *kd, *vd;        //   and block scales [B][L][KV][rows][hd / 32], rows = cap rounded up to 16
     const int32_t *seqmap;        // cache sequence of each column (nullptr: column b is sequence b)
     const int32_t *positions;
     float *o;  // [B][qd]
@@ -128,6 +128,7 @@ struct KvqCache {
     int8_t *kq, *vq;
     __half *kd, *vd;
     int L, KV, cap;
+    int rows;  // rows of each head's planes: cap rounded up to 16 (whole V tiles)
 };
 // fp16 token-major rows [n][KV * hd] (device) -> cache rows start.. of (seq, layer)
 cudaError_t launch_kvq_write(const __half *k_rows, const __half *v_rows, int n, const KvqCache &c, int hd, int seq,

@@ -49,28 +49,23 @@ struct TaCfg {
     static constexpr int SMEM = TA_WARPS * TA_SLOTS * SLOT;
 };
 
-// Q8_0 cache tiles (kernels_kvq.cu layout): per slot the K and V tiles' quantised bytes [TA_TILE][HD] and
-// scales [TA_TILE][HD / 32]; each warp also has one fp16 tile pair (K, V) in the fp16 path's layout, into
-// which it converts the quantised values (exact) before the tensor-core products.
+// Q8_0 cache tiles: whole 16-row tiles of the planes (kernels_kvq.cu order), per slot the K codes, the K
+// scales [16][HD / 32], the V codes and the V scales.  The codes are already in tensor-core fragment order:
+// a lane's B fragments of a tile are 32-bit words of one contiguous run (K: hd / 4 bytes of each of its two
+// rows; V: hd / 2 bytes), turned into exact fp16 pairs in registers.  16-byte chunks are XOR-swizzled so
+// that the 8 lanes of every 128-bit read phase hit distinct bank groups.
 template <int HD>
 struct TaQ8Cfg {
-    static constexpr int QT = TA_TILE * HD;             // quantised bytes of one tile
+    static constexpr int QT = TA_TILE * HD;             // code bytes of one tile
     static constexpr int SROW = HD / 32 * 2;            // scale bytes of one row: 8 or 4
     static constexpr int ST = TA_TILE * SROW;           // scale bytes of one tile
-    static constexpr int SLOT = 2 * (QT + ST);          // K then V: bytes, then scales
-    static constexpr int SLOTS = TA_SLOTS;              // tiles staged per warp
-    static constexpr int CONV = 2 * TaCfg<HD>::TILEB;   // the warp's converted fp16 K and V tiles
-    static constexpr int WARP = SLOTS * SLOT + CONV;
+    static constexpr int SLOT = 2 * (QT + ST);          // K codes, K scales, V codes, V scales
+    static constexpr int SLOTS = 4;                     // tiles staged per warp
+    static constexpr int NQ = HD / 32;                  // 16-byte chunks of a lane's V run
+    static constexpr int WARP = SLOTS * SLOT;
     static constexpr int SMEM = TA_WARPS * WARP;
     static constexpr float VPRE = 256.f;  // power of two the V-scaled probabilities are multiplied by
 };
-
-ER_DEV void cp_async_ca(uint32_t dst, const void *src, uint32_t src_bytes, int size) {
-    if (size == 8)
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-    else
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
 
 ER_DEV void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -133,12 +128,14 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
     using C = TaCfg<HD>;
     using Q = TaQ8Cfg<HD>;
     const int g = lane >> 2, t = lane & 3;
-    const int ntiles = (r1 - r0 + TA_TILE - 1) / TA_TILE;
+    // fp16: tiles from r0; Q8: the whole 16-row tiles of the planes that cover [r0, r1)
+    const int tb0 = Q8 ? r0 & ~(TA_TILE - 1) : r0;
+    const int ntiles = (r1 - tb0 + TA_TILE - 1) / TA_TILE;
     const uint32_t ring_s = smem_u32(ring);
     constexpr int NS = Q8 ? Q::SLOTS : TA_SLOTS;  // ring slots
     auto issue = [&](int k) {
         if (k < ntiles) {
-            const int rb = r0 + k * TA_TILE;
+            const int rb = tb0 + k * TA_TILE;
             if constexpr (!Q8) {
                 const uint32_t slot = ring_s + (uint32_t)((k % TA_SLOTS) * C::SLOT);
 #pragma unroll
@@ -152,22 +149,23 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
                     cp_async16(slot + C::TILEB + d, src.V + off, ok ? 16u : 0u);
                 }
             } else {
-                // quantised bytes: 16-byte chunks, row-major [TA_TILE][HD]; scales: one copy per row
+                // a whole tile of the planes (rows rb .. rb + 15 lie below the planes' rounded-up rows)
                 const uint32_t slot = ring_s + (uint32_t)((k % NS) * Q::SLOT);
 #pragma unroll
-                for (int i = 0; i < Q::QT / 16 / 32; ++i) {
-                    const int ci = lane + 32 * i, row = ci / (HD / 16), col = ci % (HD / 16);
-                    const bool ok = rb + row < r1;
-                    const size_t off = (size_t)(ok ? rb + row : r0) * HD + col * 16;
-                    cp_async16(slot + ci * 16, src.Kq + off, ok ? 16u : 0u);
-                    cp_async16(slot + Q::QT + Q::ST + ci * 16, src.Vq + off, ok ? 16u : 0u);
+                for (int i = 0; i < HD / 32; ++i) {
+                    const int ci = lane + 32 * i;  // 16-byte chunk of the tile (HD chunks per side)
+                    const int row = ci / (HD / 16), j = ci % (HD / 16);
+                    cp_async16(slot + row * HD + ((j ^ (row & 1)) << 4), src.Kq + (size_t)(rb + row) * HD + j * 16,
+                               16u);
+                    const int L = ci / Q::NQ, q = ci % Q::NQ, key = (L * Q::NQ / 8) % Q::NQ;
+                    cp_async16(slot + Q::QT + Q::ST + L * (HD / 2) + ((q ^ key) << 4),
+                               src.Vq + (size_t)rb * HD + ci * 16, 16u);
                 }
-                if (lane < 2 * TA_TILE) {
-                    const int row = lane & (TA_TILE - 1), kv = lane >> 4;
-                    const bool ok = rb + row < r1;
-                    const size_t off = (size_t)(ok ? rb + row : r0) * (HD / 32);
-                    cp_async_ca(slot + kv * (Q::QT + Q::ST) + Q::QT + row * Q::SROW, (kv ? src.Vd : src.Kd) + off,
-                                ok ? (uint32_t)Q::SROW : 0u, Q::SROW);
+                if (lane < Q::SROW) {  // scales: 16 rows x SROW bytes per side, SROW chunks
+                    cp_async16(slot + Q::QT + lane * 16, src.Kd + (size_t)rb * (HD / 32) + lane * 8, 16u);
+                } else if (lane >= 16 && lane < 16 + Q::SROW) {
+                    cp_async16(slot + 2 * Q::QT + Q::ST + (lane - 16) * 16,
+                               src.Vd + (size_t)rb * (HD / 32) + (lane - 16) * 8, 16u);
                 }
             }
         }
@@ -227,7 +225,6 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
     const int sw = lane & 7;
     const uint32_t k_row = (uint32_t)(((lane & 7) + ((lane >> 4) << 3)) * C::ROWB), k_half = (lane >> 3) & 1;
     const uint32_t v_row = (uint32_t)(C::TILEB + ((lane & 7) + (((lane >> 3) & 1) << 3)) * C::ROWB), v_half = lane >> 4;
-    const uint32_t conv = ring_s + NS * Q::SLOT;  // Q8: this warp's converted fp16 tiles
     for (int k = 0; k < ntiles; ++k) {
         issue(k + NS - 1);
         cp_async_wait<NS - 1>();
@@ -248,24 +245,19 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
             }
         } else {
             const uint32_t qslot = ring_s + (uint32_t)((k % NS) * Q::SLOT);
-            // the quantised K and V tiles into fp16 (exact), in the fp16 path's swizzled layout: each lane
-            // takes 8 codes (one fp16 chunk), so that the 8 lanes of each store phase fill 8 distinct chunks
+            // this lane's K words: rows g and g + 8, dims 16c + {2t, 2t+1, 2t+8, 2t+9} of chunk c
+            uint32_t kw[2][HD / 16];
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv)
+            for (int h = 0; h < 2; ++h) {
+                const int row = 8 * h + g;
 #pragma unroll
-                for (int i = 0; i < Q::QT / 8 / 32; ++i) {
-                    const int ci = lane + 32 * i, row = ci / (HD / 8), col = ci % (HD / 8);
-                    uint32_t w0, w1;
-                    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                                 : "=r"(w0), "=r"(w1)
-                                 : "r"(qslot + kv * (Q::QT + Q::ST) + ci * 8));
-                    uint32_t h[4];
-                    q8_word_to_h2(w0 ^ 0x80808080u, h[0], h[1]);
-                    q8_word_to_h2(w1 ^ 0x80808080u, h[2], h[3]);
-                    const uint32_t dst = conv + kv * C::TILEB + row * C::ROWB + ((col ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[0]), "r"(h[1]), "r"(h[2]),
-                                 "r"(h[3]) : "memory");
+                for (int k2 = 0; k2 < HD / 64; ++k2) {
+                    const int ch = (HD / 64) * t + k2;
+                    const uint4 w = lds128(qslot + row * HD + ((ch ^ (row & 1)) << 4));
+                    kw[h][4 * k2] = w.x; kw[h][4 * k2 + 1] = w.y; kw[h][4 * k2 + 2] = w.z; kw[h][4 * k2 + 3] = w.w;
                 }
+            }
+            // the K / V scales of this lane's four rows 2t, 2t + 1, 2t + 8, 2t + 9 (fp16 pairs)
             const int rows4[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -276,11 +268,10 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
                     dks[i][w] = x;
                     asm volatile("ld.shared.u32 %0, [%1];"
                                  : "=r"(x)
-                                 : "r"(qslot + Q::QT + Q::ST + Q::QT + rows4[i] * Q::SROW + 4 * w));
+                                 : "r"(qslot + 2 * Q::QT + Q::ST + rows4[i] * Q::SROW + 4 * w));
                     dvs[i][w] = x;
                 }
-            __syncwarp();
-            slot = conv;
+            slot = qslot;
             // scores block by block (2 k16 chunks per 32-value block), each block's sums times its row's scale
 #pragma unroll
             for (int bb = 0; bb < HD / 32; ++bb) {
@@ -288,7 +279,8 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
 #pragma unroll
                 for (int c = 2 * bb; c < 2 * bb + 2; ++c) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(slot + k_row + (((2 * c + k_half) ^ sw) << 4), b0, b1, b2, b3);
+                    q8_word_to_h2(kw[0][c] ^ 0x80808080u, b0, b1);
+                    q8_word_to_h2(kw[1][c] ^ 0x80808080u, b2, b3);
                     mma_16816(b0s, qa[c], b0, b1, b0s);
                     mma_16816(b1s, qa[c], b2, b3, b1s);
                 }
@@ -301,13 +293,13 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
                 s1[1] = fmaf(dk[3], b1s[1], s1[1]); s1[3] = fmaf(dk[3], b1s[3], s1[3]);
             }
         }
-        const int rb = r0 + k * TA_TILE;
+        const int rb = tb0 + k * TA_TILE;
         float sc[4] = {(s0[0] + s0[2]) * down, (s0[1] + s0[3]) * down, (s1[0] + s1[2]) * down,
                        (s1[1] + s1[3]) * down};
         const int rr[4] = {rb + 2 * t, rb + 2 * t + 1, rb + 2 * t + 8, rb + 2 * t + 9};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            if (rr[i] >= r1) sc[i] = -INFINITY;
+            if (rr[i] >= r1 || rr[i] < r0) sc[i] = -INFINITY;
         float mt = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
@@ -344,6 +336,16 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
                 mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
             }
         } else {
+            // this lane's V words: rows {2t, 2t+1, 2t+8, 2t+9} of dim 8j + g for every n8 tile j
+            uint32_t vw[HD / 8];
+            {
+                const int key = (lane * Q::NQ / 8) % Q::NQ;
+#pragma unroll
+                for (int q = 0; q < Q::NQ; ++q) {
+                    const uint4 w = lds128(slot + Q::QT + Q::ST + lane * (HD / 2) + ((q ^ key) << 4));
+                    vw[4 * q] = w.x; vw[4 * q + 1] = w.y; vw[4 * q + 2] = w.z; vw[4 * q + 3] = w.w;
+                }
+            }
             // per 32-value block of V: P times the block's row scales (and 2^8, so that the fp16 halves
             // stay normal), split hi + lo, against the block's four n8 tiles
 #pragma unroll
@@ -359,11 +361,10 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
                 const uint32_t pa[4] = {pack_h2(ph[0], ph[1]), pack_h2(pl[0], pl[1]), pack_h2(ph[2], ph[3]),
                                         pack_h2(pl[2], pl[3])};
 #pragma unroll
-                for (int j2 = 2 * bb; j2 < 2 * bb + 2; ++j2) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(slot + v_row + (((2 * j2 + v_half) ^ sw) << 4), b0, b1, b2, b3);
-                    mma_16816(st.o[2 * j2], pa, b0, b1, st.o[2 * j2]);
-                    mma_16816(st.o[2 * j2 + 1], pa, b2, b3, st.o[2 * j2 + 1]);
+                for (int j = 4 * bb; j < 4 * bb + 4; ++j) {
+                    uint32_t b0, b1;
+                    q8_word_to_h2(vw[j] ^ 0x80808080u, b0, b1);
+                    mma_16816(st.o[j], pa, b0, b1, st.o[j]);
                 }
             }
         }
@@ -421,11 +422,12 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArg
         const size_t head = ((size_t)(a.seqmap ? a.seqmap[b] : b) * a.L + a.layer) * a.KV + kvh;
         TaSrc src;
         if constexpr (Q8) {
+            const size_t rows = (size_t)((a.cap + TA_TILE - 1) & ~(TA_TILE - 1));  // whole tiles per head
             src.K = src.V = nullptr;
-            src.Kq = a.kq + head * a.cap * HD;
-            src.Vq = a.vq + head * a.cap * HD;
-            src.Kd = a.kd + head * a.cap * (HD / 32);
-            src.Vd = a.vd + head * a.cap * (HD / 32);
+            src.Kq = a.kq + head * rows * HD;
+            src.Vq = a.vq + head * rows * HD;
+            src.Kd = a.kd + head * rows * (HD / 32);
+            src.Vd = a.vd + head * rows * (HD / 32);
         } else {
             src.K = a.kc + head * a.cap * HD;
             src.V = a.vc + head * a.cap * HD;

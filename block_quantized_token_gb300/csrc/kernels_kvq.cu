@@ -5,9 +5,18 @@
 // End-to-End Inference Path", P9 quantized-KV flash-attention variants and
 // section 5; "EdgeRunner Core Architecture" section 4.1 cache precisions) but
 // give no quantiser for it.  Each head's row of hd values is stored as hd/32
-// Q8_0 blocks, in two planes per (sequence, layer, KV head):
-//   q  int8 [capacity][hd]        the quantised values
-//   d  fp16 [capacity][hd / 32]   one scale per 32-value block
+// Q8_0 blocks, in two planes per (sequence, layer, KV head), with `rows` =
+// capacity rounded up to 16:
+//   q  int8 [rows * hd]        the codes, in the order the attention kernel's
+//                              tensor-core fragments take them (below)
+//   d  fp16 [rows][hd / 32]    one scale per 32-value block
+// K codes: row-major, each row's hd bytes permuted so that lane t of an MMA
+// quad finds its four values of every 16-value chunk c (dims 16c + 2t, + 1,
+// + 8, + 9) as one 32-bit word, and its words of all chunks as one run of
+// hd / 4 bytes.  V codes: in tiles of 16 rows, each tile ordered
+// [dim % 8][quad lane][dim / 8][4 bytes of rows 2t, 2t + 1, 2t + 8, 2t + 9], so that
+// a lane's P.V fragments of the whole tile are one run of hd / 2 bytes.
+// er_kv_read_blocks returns the GGUF blocks in their own order.
 // Quantiser (every step in float32, the same on every path that writes the
 // cache): amax = largest |x| of the block; d = fp16(amax / 127) (float32
 // division, round to nearest even); q = clamp(round(x / d), -127, 127) with
@@ -18,11 +27,26 @@
 
 namespace er {
 
+// byte offset of dim d within a K row, and of (row r of its tile, dim d) within a V tile
+__host__ __device__ inline int kvq_kpos(int d, int hd) {
+    const int c = d >> 4, w = d & 15;
+    return ((w & 7) >> 1) * (hd / 4) + c * 4 + ((w & 1) | ((w >> 3) << 1));
+}
+__host__ __device__ inline int kvq_vpos(int r, int d, int hd) {
+    const int t = (r & 7) >> 1, s = (r & 1) | ((r >> 3) << 1);
+    return (((d & 7) * 4 + t) * (hd / 8) + (d >> 3)) * 4 + s;
+}
+// byte offset of (row r, dim d) in one head's code plane of either side
+__host__ __device__ inline size_t kvq_code_off(bool v, int r, int d, int hd) {
+    return v ? (size_t)(r >> 4) * 16 * hd + kvq_vpos(r & 15, d, hd) : (size_t)r * hd + kvq_kpos(d, hd);
+}
+
 // One head row held by a warp, E = hd / 32 consecutive values per lane (lane l:
 // values E l .. E l + E - 1); a 32-value block spans 32 / E lanes.  Writes the
-// row's q (E bytes per lane) and its scales.
+// row's codes (E bytes per lane, at their places in the head's plane `q_head`)
+// and its scales.
 template <int E>
-__device__ inline void kvq_row(const float (&x)[E], int8_t *q_row, __half *d_row, int lane) {
+__device__ inline void kvq_row(const float (&x)[E], int8_t *q_head, bool v, int r, __half *d_row, int lane) {
     float amax = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
@@ -31,17 +55,12 @@ __device__ inline void kvq_row(const float (&x)[E], int8_t *q_row, __half *d_row
     for (int off = 1; off < 32 / E; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const __half dh = __float2half_rn(amax / 127.f);
     const float d = __half2float(dh);
-    uint32_t packed = 0;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        float r = d > 0.f ? roundf(x[e] / d) : 0.f;
-        r = fminf(fmaxf(r, -127.f), 127.f);
-        packed |= ((uint32_t)(uint8_t)(int8_t)(int)r) << (8 * e);
+        float q = d > 0.f ? roundf(x[e] / d) : 0.f;
+        q = fminf(fmaxf(q, -127.f), 127.f);
+        q_head[kvq_code_off(v, r, E * lane + e, 32 * E)] = (int8_t)(int)q;
     }
-    if (E == 4)
-        reinterpret_cast<uint32_t *>(q_row)[lane] = packed;
-    else
-        reinterpret_cast<uint16_t *>(q_row)[lane] = (uint16_t)packed;
     if ((lane & (32 / E - 1)) == 0) d_row[lane / (32 / E)] = dh;
 }
 
@@ -62,8 +81,9 @@ __global__ void kvq_write_kernel(const __half *k_rows, const __half *v_rows, int
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] = __half2float(src[e]);
     const size_t head = kvq_head(seq, c.L, layer, c.KV, h);
-    const size_t r = head * c.cap + start + row;
-    kvq_row<E>(x, (kv ? c.vq : c.kq) + r * hd, (kv ? c.vd : c.kd) + r * (hd / 32), lane);
+    const int r = start + row;
+    kvq_row<E>(x, (kv ? c.vq : c.kq) + head * c.rows * hd, kv != 0, r,
+               (kv ? c.vd : c.kd) + (head * c.rows + r) * (hd / 32), lane);
 }
 
 // The step's new rows: fp32 staging [B][KV * hd] (written by the Q/K/V epilogue) -> cache row
@@ -85,8 +105,9 @@ __global__ void kvq_stage_kernel(const float *k_stage, const float *v_stage, con
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] = __ldcg(src + e);
-    const size_t r = kvq_head(seqmap ? seqmap[b] : b, c.L, layer, c.KV, h) * c.cap + pos;
-    kvq_row<E>(x, (kv ? c.vq : c.kq) + r * hd, (kv ? c.vd : c.kd) + r * (hd / 32), lane);
+    const size_t head = kvq_head(seqmap ? seqmap[b] : b, c.L, layer, c.KV, h);
+    kvq_row<E>(x, (kv ? c.vq : c.kq) + head * c.rows * hd, kv != 0, pos,
+               (kv ? c.vd : c.kd) + (head * c.rows + pos) * (hd / 32), lane);
 }
 
 // cache rows start..start+n-1 of (seq, layer) -> token-major GGUF Q8_0 blocks [n][KV * hd / 32][34 bytes]
@@ -99,13 +120,14 @@ __global__ void kvq_read_kernel(uint8_t *k_out, uint8_t *v_out, int n, KvqCache 
         const long long rem = i - (long long)kv * n * nb * 34;
         const int row = (int)(rem / (nb * 34)), j = (int)(rem % (nb * 34));
         const int blk = j / 34, byte = j % 34, h = blk / (hd / 32), hb = blk % (hd / 32);
-        const size_t r = kvq_head(seq, c.L, layer, c.KV, h) * c.cap + start + row;
+        const size_t head = kvq_head(seq, c.L, layer, c.KV, h);
+        const int r = start + row;
         uint8_t out;
         if (byte < 2) {
-            const __half d = (kv ? c.vd : c.kd)[r * (hd / 32) + hb];
+            const __half d = (kv ? c.vd : c.kd)[(head * c.rows + r) * (hd / 32) + hb];
             out = (uint8_t)(__half_as_ushort(d) >> (8 * byte));
         } else {
-            out = (uint8_t)(kv ? c.vq : c.kq)[r * hd + hb * 32 + byte - 2];
+            out = (uint8_t)(kv ? c.vq : c.kq)[head * c.rows * hd + kvq_code_off(kv != 0, r, hb * 32 + byte - 2, hd)];
         }
         (kv ? v_out : k_out)[(size_t)rem] = out;
     }
