@@ -32,7 +32,9 @@
 
 namespace er {
 
-constexpr int TA_WARPS = 8;
+constexpr int TA_WARPS = 8;     // warps per CTA, fp16 cache
+constexpr int TA_WARPS_Q8 = 8;  // warps per CTA, Q8_0 cache
+constexpr int ta_warps(bool q8) { return q8 ? TA_WARPS_Q8 : TA_WARPS; }
 constexpr int TA_SLOTS = 3;
 constexpr int TA_TILE = 16;
 constexpr int TA_MIN_ROWS = 64;  // rows per warp at least
@@ -63,7 +65,7 @@ struct TaQ8Cfg {
     static constexpr int SLOTS = 4;                     // tiles staged per warp
     static constexpr int NQ = HD / 32;                  // 16-byte chunks of a lane's V run
     static constexpr int WARP = SLOTS * SLOT;
-    static constexpr int SMEM = TA_WARPS * WARP;
+    static constexpr int SMEM = TA_WARPS_Q8 * WARP;
     static constexpr float VPRE = 256.f;  // power of two the V-scaled probabilities are multiplied by
 };
 
@@ -384,7 +386,7 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
 }
 
 template <int HD, int G, bool Q8>
-__global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const AttnArgs a) {
     using C = TaCfg<HD>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -405,10 +407,10 @@ __global__ void __launch_bounds__(TA_WARPS * 32, 1) attn_tc_kernel(const AttnArg
         geo.NR += a.KV * geo.T[b];
     }
     geo.base[a.B] = geo.NR;
-    const int Wmax = gridDim.x * TA_WARPS;
+    const int Wmax = gridDim.x * ta_warps(Q8);
     geo.W = (geo.NR + TA_MIN_ROWS - 1) / TA_MIN_ROWS;
     if (geo.W > Wmax) geo.W = Wmax;
-    const int w = blockIdx.x * TA_WARPS + warp;
+    const int w = blockIdx.x * ta_warps(Q8) + warp;
     if (w >= geo.W) return;
     const int wa = (int)((long long)w * geo.NR / geo.W), wb = (int)((long long)(w + 1) * geo.NR / geo.W);
 
@@ -522,7 +524,9 @@ void attention_plan(int hd, int KV, int B, int cap, int num_sms, int *S, int *CH
     *CH = TA_MIN_ROWS;   // rows per warp at least
 }
 
-size_t attention_part_floats(int hd, int G, int num_sms) { return (size_t)num_sms * TA_WARPS * 2 * G * (hd + 4); }
+size_t attention_part_floats(int hd, int G, int num_sms) {
+    return (size_t)num_sms * (TA_WARPS > TA_WARPS_Q8 ? TA_WARPS : TA_WARPS_Q8) * 2 * G * (hd + 4);
+}
 
 template <int HD, int G>
 static cudaError_t at_launch(const AttnArgs &a, cudaStream_t st, bool pdl) {
@@ -530,7 +534,7 @@ static cudaError_t at_launch(const AttnArgs &a, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3((unsigned)a.S);
-    cfg.blockDim = dim3(TA_WARPS * 32);
+    cfg.blockDim = dim3(ta_warps(q8) * 32);
     cfg.dynamicSmemBytes = q8 ? TaQ8Cfg<HD>::SMEM : TaCfg<HD>::SMEM;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
