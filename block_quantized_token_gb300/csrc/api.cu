@@ -573,7 +573,9 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
             a.v_stage = kv->vstage;
             a.seqmap = kv->seqmap;
             cudaError_t e = gemv_all(kv, EPI_QKV, a, st, pdl);
-            if (e == cudaSuccess && kv->kv_type == ER_Q8_0)
+            // Q8_0 cache: the attention kernel quantises each sequence's new rows itself, except in a prefill
+            // chunk, whose columns read each other's new rows: those are quantised first, by their own launch
+            if (e == cudaSuccess && kv->kv_type == ER_Q8_0 && kv->seqmap)
                 e = launch_kvq_stage(kv->kstage, kv->vstage, positions, kv->seqmap, kv->B, kv->kvq, c.head_dim, l,
                                      st, pdl);
             return e;
@@ -588,6 +590,10 @@ static cudaError_t enqueue_stage(er_kv *kv, int stage, int l, const int32_t *tok
             a.kd = kv->kvq.kd;
             a.vd = kv->kvq.vd;
             a.seqmap = kv->seqmap;
+            if (kv->kv_type == ER_Q8_0 && !kv->seqmap) {
+                a.k_stage = kv->kstage;
+                a.v_stage = kv->vstage;
+            }
             a.positions = positions;
             a.o = kv->o;
             a.part = kv->attn_part;
@@ -849,8 +855,7 @@ int32_t er_kv_launches_per_step(const er_kv *kv) {
         return per > 0 ? (kv->B + per - 1) / per : 0;
     };
     const er_layer_dev &L0 = m->layers[0];
-    const int per_layer = groups(L0.qkv) + (kv->kv_type == ER_Q8_0 ? 1 : 0) + 1 + groups(L0.wo) + groups(L0.gateup) +
-                          groups(L0.down);
+    const int per_layer = groups(L0.qkv) + 1 + groups(L0.wo) + groups(L0.gateup) + groups(L0.down);
     return 1 + c.n_layers * per_layer + groups(m->head);
 }
 

@@ -110,6 +110,8 @@ struct AttnArgs {
     const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): codes [B][L][KV][rows * hd] (kernels_kvq.cu order)
     const __half *kd, *vd;        //   and block scales [B][L][KV][rows][hd / 32], rows = cap rounded up to 16
     const int32_t *seqmap;        // cache sequence of each column (nullptr: column b is sequence b)
+    const float *k_stage, *v_stage;  // Q8_0: the new rows in fp32 [B][KV * hd], quantised by the kernel (or
+                                     // nullptr: already in the planes)
     const int32_t *positions;
     float *o;  // [B][qd]
     float *part;  // warp states of pairs shared by warps (attention_part_floats)

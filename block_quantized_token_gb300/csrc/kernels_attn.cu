@@ -29,6 +29,7 @@
 // two are requested before its queries are read.
 #include "common.cuh"
 #include "internal.h"
+#include "kvq.cuh"
 
 namespace er {
 
@@ -435,6 +436,26 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
             src.V = a.vc + head * a.cap * HD;
             src.Kq = src.Vq = nullptr;
             src.Kd = src.Vd = nullptr;
+        }
+        if constexpr (Q8) {
+            // the step's new row (the pair's last) from the fp32 staging into the planes, by the one warp
+            // whose range holds it, before any of its tiles is requested.  Other warps may stage the same
+            // 16-row tile meanwhile; the row lies outside their ranges and is masked there.
+            if (a.k_stage && r1 == seg_end - seg_start) {
+                constexpr int E = HD / 32;
+                const int pos = r1 - 1;
+#pragma unroll
+                for (int kvs = 0; kvs < 2; ++kvs) {
+                    const float *xs = (kvs ? a.v_stage : a.k_stage) + ((size_t)b * a.KV + kvh) * HD + E * lane;
+                    float x[E];
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[e] = __ldcg(xs + e);
+                    kvq_row<E>(x, const_cast<int8_t *>(kvs ? src.Vq : src.Kq), kvs != 0, pos,
+                               const_cast<__half *>(kvs ? src.Vd : src.Kd) + (size_t)pos * (HD / 32), lane);
+                }
+                __threadfence();
+                __syncwarp();
+            }
         }
         TaState<HD> st;
         ta_attend<HD, G, Q8>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, src, r0, r1, ring, lane, st);

@@ -232,8 +232,7 @@ ER_API er_status er_kv_set_wide_gemv(er_kv *kv, int32_t variant);
 /* Kernel launches one er_decode_step enqueues under the schedule in effect
  * (memsets not counted), or -1 for NULL: 1 for the persistent schedule; for
  * the per-phase one, the embedding, per layer the QKV, attention, Wo, gate/up
- * and down launches (and, on an ER_Q8_0 cache, the quantisation of the new
- * K/V rows), and the head.  A GEMV is one launch for batches up to 4
+ * and down launches, and the head.  A GEMV is one launch for batches up to 4
  * and for batches of 5..16 whose matrices take the one-pass batched kernel
  * (K a multiple of 64); otherwise one launch per group of at most 4 batch
  * columns that fit its shared memory. */
