@@ -107,7 +107,7 @@ int gemv_max_cols(int qt, int K);  // largest B <= 4 that gemv_fits
 struct AttnArgs {
     const float *q;  // [B][qd]
     const __half *kc, *vc;        // fp16 cache [B][L][KV][cap][hd], or
-    const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): codes [B][L][KV][rows * hd] (kernels_kvq.cu order)
+    const int8_t *kq, *vq;        // Q8_0 cache (kq != nullptr): codes [B][L][KV][rows * hd] (kvq.cuh order)
     const __half *kd, *vd;        //   and block scales [B][L][KV][rows][hd / 32], rows = cap rounded up to 16
     const int32_t *seqmap;        // cache sequence of each column (nullptr: column b is sequence b)
     const float *k_stage, *v_stage;  // Q8_0: the new rows in fp32 [B][KV * hd], quantised by the kernel (or
@@ -135,7 +135,7 @@ struct KvqCache {
 // fp16 token-major rows [n][KV * hd] (device) -> cache rows start.. of (seq, layer)
 cudaError_t launch_kvq_write(const __half *k_rows, const __half *v_rows, int n, const KvqCache &c, int hd, int seq,
                              int layer, int start, cudaStream_t st);
-// the step's fp32 staging rows [B][KV * hd] -> cache row positions[b] of `layer`
+// a prefill chunk's fp32 staging rows [B][KV * hd] -> cache row positions[b] of sequence seqmap[b], `layer`
 cudaError_t launch_kvq_stage(const float *k_stage, const float *v_stage, const int32_t *positions,
                              const int32_t *seqmap, int B, const KvqCache &c, int hd, int layer, cudaStream_t st,
                              bool pdl);

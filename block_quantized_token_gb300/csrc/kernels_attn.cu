@@ -450,6 +450,7 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
                     float x[E];
 #pragma unroll
                     for (int e = 0; e < E; ++e) x[e] = __ldcg(xs + e);
+                    // the planes are read-only to the tiles' loads, written here once per step
                     kvq_row<E>(x, const_cast<int8_t *>(kvs ? src.Vq : src.Kq), kvs != 0, pos,
                                const_cast<__half *>(kvs ? src.Vd : src.Kd) + (size_t)pos * (HD / 32), lane);
                 }

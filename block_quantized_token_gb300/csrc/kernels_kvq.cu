@@ -27,9 +27,10 @@ __global__ void kvq_write_kernel(const __half *k_rows, const __half *v_rows, int
                (kv ? c.vd : c.kd) + (head * c.rows + r) * (hd / 32), lane);
 }
 
-// The step's new rows: fp32 staging [B][KV * hd] (written by the Q/K/V epilogue) -> cache row
+// A prefill chunk's new rows: fp32 staging [B][KV * hd] (written by the Q/K/V epilogue) -> cache row
 // positions[b] of sequence seqmap[b] (b without a map) of layer `layer`, for every column whose
-// position is in range; one warp per (column, head, K or V).
+// position is in range; one warp per (column, head, K or V).  (In a decode step the attention kernel
+// quantises the new rows itself.)
 template <int E>
 __global__ void kvq_stage_kernel(const float *k_stage, const float *v_stage, const int32_t *positions,
                                  const int32_t *seqmap, int B, KvqCache c, int layer) {
