@@ -104,8 +104,8 @@ KERNEL_TRAFFIC = {
     ("smollm_q8", "step_kernel"): ("35d7ab1969b026e2", 190641152 + 3227648),
     # attn_tc_kernel<128, 4, fp16 / Q8_0 cache>, 4th launch of `bench.py [--workload llama3_8b_q8_b16_kvq8]
     # --layers 1 --steps 1 --warmup 3 --no-cpu-baseline` (one layer: the per-layer shape of the full model)
-    ("llama3_8b_q8_b16", "attn"): ("38052aa7bf3d8f34", 537800704 + 9338368),
-    ("llama3_8b_q8_b16_kvq8", "attn"): ("38052aa7bf3d8f34", 286342400 + 9010688),
+    ("llama3_8b_q8_b16", "attn"): ("0c0af277057d46b2", 537762304 + 9601536),
+    ("llama3_8b_q8_b16_kvq8", "attn"): ("0c0af277057d46b2", 291742976 + 9256704),
 }
 
 
