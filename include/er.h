@@ -148,8 +148,11 @@ ER_API int32_t er_kv_type(const er_kv *kv);
  * allocates a 16-column scratch (activations and partials, about as much as a
  * 16-sequence decode state without its cache) and synchronises the device; it is
  * freed with kv.  Bad tokens and positions set the flags er_get_device_error
- * reports.  ER_EINVAL: kv NULL, seq out of range, start < 0, n < 0,
- * start + n > capacity, or tokens_dev NULL with n > 0. */
+ * reports.  It writes the rows it is given and reads the sequence's rows
+ * below them: do not run it concurrently (on another stream) with a decode
+ * step or another prefill of the same kv.  ER_EINVAL: kv NULL, seq out of
+ * range, start < 0, n < 0, start + n > capacity, or tokens_dev NULL with
+ * n > 0. */
 ER_API er_status er_prefill(er_kv *kv, int32_t seq, const int32_t *tokens_dev, int32_t n, int32_t start,
                             float *logits_dev, void *stream);
 
