@@ -100,8 +100,10 @@ STEP_KERNEL_SOURCES = KERNEL_SOURCES["step_kernel"]
 # reports no traffic until it is captured again.  Captures of a cut model (fewer layers) are per launch
 # of the same kernel on the same per-layer shapes.
 KERNEL_TRAFFIC = {
-    # step_kernel<Q8_0, 64, 3>, 4th launch of `bench.py --workload smollm_q8 --steps 4 --warmup 3 --no-cpu-baseline`
-    ("smollm_q8", "step_kernel"): ("35d7ab1969b026e2", 190641152 + 3227648),
+    # step_kernel<Q8_0, 64, 3> / <Q4_0, 128, 1>, 4th launch of `bench.py --workload smollm_q8 | llama2_7b_q4
+    # --steps 4 --warmup 3 --no-cpu-baseline` (full size, one pass)
+    ("smollm_q8", "step_kernel"): ("3ef517f4638baae0", 190925824 + 3020032),
+    ("llama2_7b_q4", "step_kernel"): ("3ef517f4638baae0", 5866404352 + 9216768),
     # attn_tc_kernel<128, 4, fp16 / Q8_0 cache>, 4th launch of `bench.py [--workload llama3_8b_q8_b16_kvq8]
     # --layers 1 --steps 1 --warmup 3 --no-cpu-baseline` (one layer: the per-layer shape of the full model)
     ("llama3_8b_q8_b16", "attn"): ("0c0af277057d46b2", 537762304 + 9601536),
