@@ -140,64 +140,6 @@ def test_q8_cache_api_rules():
 # ------------------------------------------------------------------------------------------
 # chains: the legitimate one-code differences of the new rows, and their effect on the logits
 # ------------------------------------------------------------------------------------------
-def _codes(xb, d):
-    """The quantiser's codes of one block for a given fp16 scale d (float32 quotient, half away from zero)."""
-    d32 = np.float32(d)
-    r = np.zeros_like(xb, dtype=np.float32) if d32 == 0 else (xb.astype(np.float32) / d32).astype(np.float64)
-    return np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
-
-
-def _alternatives(x, delta):
-    """Each way the quantiser may code a block of the row x (float64 [n]) differently from the oracle for some
-    row within delta of x: (block, d, q) with one code one step off where x / d lies within reach of a
-    half-integer, or the whole block under the other fp16 scale where amax / 127 lies within reach of an
-    fp16 rounding boundary.  Same margin as helpers.check_q8_blocks."""
-    x = np.asarray(x, np.float64)
-    d_ref, q_ref = oracle.quantize_kv_q8_0(x.astype(np.float32))
-    delta = 2.0 * np.asarray(delta, np.float64) + 2.0 ** -22 * np.abs(x)
-    out = []
-    for blk in range(x.size // 32):
-        xb, db, qb = x[32 * blk:32 * blk + 32], delta[32 * blk:32 * blk + 32], q_ref[32 * blk:32 * blk + 32]
-        amax, amd = np.abs(xb).max(), db.max()
-        for d2 in {np.float16(np.float32((amax - amd) / 127)), np.float16(np.float32((amax + amd) / 127))}:
-            if d2 != d_ref[blk]:
-                out.append((blk, d2, _codes(xb.astype(np.float32), d2)))
-        d = float(d_ref[blk])
-        if d == 0:
-            continue
-        r = np.abs(xb) / d
-        near = np.abs(r - np.floor(r) - 0.5) <= db / d
-        for e in np.nonzero(near)[0]:
-            k = int(np.floor(r[e]))
-            cur = abs(int(qb[e]))
-            alt = min(k if cur == k + 1 else k + 1, 127)
-            if alt != cur:
-                q2 = qb.copy()
-                q2[e] = np.int8(np.sign(xb[e]) * alt)
-                out.append((blk, d_ref[blk], q2))
-    return out
-
-
-class _OverrideCache(oracle.OracleCache):
-    """The oracle's Q8_0 cache with one block of one new layer-0 row replaced after it is quantised."""
-
-    def __init__(self, cfg, batch, capacity, override):
-        super().__init__(cfg, batch, capacity, kv_type="q8_0")
-        self.override = override  # (b, position, "k" | "v", block, d, q)
-
-    def put(self, b, layer, rows, k, v):
-        super().put(b, layer, rows, k, v)
-        ob, op, side, blk, d2, q2 = self.override
-        if layer != 0 or not isinstance(rows, (int, np.integer)) or (b, int(rows)) != (ob, op):
-            return
-        hd = self.cfg.head_dim
-        h, j = divmod(blk, hd // 32)
-        ds, qs, full = (self.kd, self.kq, self.k) if side == "k" else (self.vd, self.vq, self.v)
-        ds[b][0][op][h, j] = d2
-        qs[b][0][op][h, 32 * j:32 * j + 32] = q2
-        full[b][0][op][h] = oracle.dequant_kv_q8_0(ds[b][0][op][h], qs[b][0][op][h]).astype(np.float32)
-
-
 def _flip_tolerance(om, wl, fed, base, positions, steps):
     """Per (step, sequence): sums over the legitimate alternatives of the new layer-0 rows (steps <= this one)
     of the max-abs and L2 change each alone makes to the oracle's logits, the next tokens held fixed."""
@@ -213,9 +155,9 @@ def _flip_tolerance(om, wl, fed, base, positions, steps):
             p = int(positions[b]) + st
             k_x, v_x, dk, dv = layer0_kv_exact(om, s, int(fed[st, b]), p)
             for side, xv, dl in (("k", k_x, dk), ("v", v_x, dv)):
-                for blk, d2, q2 in _alternatives(xv, dl):
+                for blk, d2, q2 in helpers.q8_alternatives(xv, dl):
                     n_alt += 1
-                    c = _OverrideCache(cfg, B, wl.capacity, (b, p, side, blk, d2, q2))
+                    c = helpers.OverrideCache(cfg, B, wl.capacity, (b, p, side, blk, d2, q2))
                     c.fill(b, 0, k0, v0)
                     for s2 in range(st, steps):
                         if s2 == st:  # the rows before step st are the oracle's own: replay them unchanged
