@@ -306,8 +306,10 @@ static er_status kv_create(er_model *m, int32_t batch, int32_t capacity, int32_t
     } else {
         const int rows = (capacity + 15) & ~15;  // whole tiles of 16 rows per head
         const size_t q_elems = cache_elems / capacity * rows;
-        A(&kv->kvq.kq, q_elems);
-        A(&kv->kvq.vq, q_elems);
+        A(&kv->kvq.kq, q_elems, false);  // codes are stored as q XOR 0x80: 0x80 is a zero code
+        A(&kv->kvq.vq, q_elems, false);
+        if (e == cudaSuccess) e = cudaMemset(kv->kvq.kq, 0x80, q_elems);
+        if (e == cudaSuccess) e = cudaMemset(kv->kvq.vq, 0x80, q_elems);
         A(&kv->kvq.kd, q_elems / 32 * sizeof(__half));
         A(&kv->kvq.vd, q_elems / 32 * sizeof(__half));
         kv->kvq.L = c.n_layers;

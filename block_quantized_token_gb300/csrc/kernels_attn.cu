@@ -91,6 +91,12 @@ ER_DEV uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
 }
+// (a, b) = hi + lo with hi = fp16(a, b) and lo = fp16 of the remainders, as two packed pairs
+ER_DEV void split_h2(float a, float b, uint32_t &hi, uint32_t &lo) {
+    hi = pack_h2(a, b);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+    lo = pack_h2(a - h.x, b - h.y);
+}
 
 struct TaGeom {
     int NR, W;  // rows in the list, working warps
@@ -282,8 +288,8 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
 #pragma unroll
                 for (int c = 2 * bb; c < 2 * bb + 2; ++c) {
                     uint32_t b0, b1, b2, b3;
-                    q8_word_to_h2(kw[0][c] ^ 0x80808080u, b0, b1);
-                    q8_word_to_h2(kw[1][c] ^ 0x80808080u, b2, b3);
+                    q8_word_to_h2(kw[0][c], b0, b1);
+                    q8_word_to_h2(kw[1][c], b2, b3);
                     mma_16816(b0s, qa[c], b0, b1, b0s);
                     mma_16816(b1s, qa[c], b2, b3, b1s);
                 }
@@ -351,22 +357,22 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
             }
             // per 32-value block of V: P times the block's row scales (and 2^8, so that the fp16 halves
             // stay normal), split hi + lo, against the block's four n8 tiles
+            float p8[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p8[i] = p[i] * Q::VPRE;
 #pragma unroll
             for (int bb = 0; bb < HD / 32; ++bb) {
-                float ph[4], pl[4];
+                float pv[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float dv = (bb & 1) ? h2f_hi(dvs[i][bb >> 1]) : h2f_lo(dvs[i][bb >> 1]);
-                    const float pv = p[i] * dv * Q::VPRE;
-                    ph[i] = __half2float(__float2half_rn(pv));
-                    pl[i] = pv - ph[i];
-                }
-                const uint32_t pa[4] = {pack_h2(ph[0], ph[1]), pack_h2(pl[0], pl[1]), pack_h2(ph[2], ph[3]),
-                                        pack_h2(pl[2], pl[3])};
+                for (int i = 0; i < 4; ++i)
+                    pv[i] = p8[i] * ((bb & 1) ? h2f_hi(dvs[i][bb >> 1]) : h2f_lo(dvs[i][bb >> 1]));
+                uint32_t pa[4];
+                split_h2(pv[0], pv[1], pa[0], pa[1]);
+                split_h2(pv[2], pv[3], pa[2], pa[3]);
 #pragma unroll
                 for (int j = 4 * bb; j < 4 * bb + 4; ++j) {
                     uint32_t b0, b1;
-                    q8_word_to_h2(vw[j] ^ 0x80808080u, b0, b1);
+                    q8_word_to_h2(vw[j], b0, b1);
                     mma_16816(st.o[j], pa, b0, b1, st.o[j]);
                 }
             }

@@ -69,7 +69,8 @@ __global__ void kvq_read_kernel(uint8_t *k_out, uint8_t *v_out, int n, KvqCache 
             const __half d = (kv ? c.vd : c.kd)[(head * c.rows + r) * (hd / 32) + hb];
             out = (uint8_t)(__half_as_ushort(d) >> (8 * byte));
         } else {
-            out = (uint8_t)(kv ? c.vq : c.kq)[head * c.rows * hd + kvq_code_off(kv != 0, r, hb * 32 + byte - 2, hd)];
+            out = (uint8_t)(kv ? c.vq : c.kq)[head * c.rows * hd + kvq_code_off(kv != 0, r, hb * 32 + byte - 2, hd)] ^
+                  0x80u;
         }
         (kv ? v_out : k_out)[(size_t)rem] = out;
     }

@@ -16,6 +16,7 @@
 // hd / 4 bytes.  V codes: in tiles of 16 rows, each tile ordered
 // [dim % 8][quad lane][dim / 8][4 bytes of rows 2t, 2t + 1, 2t + 8, 2t + 9], so that
 // a lane's P.V fragments of the whole tile are one run of hd / 2 bytes.
+// Each code byte holds q XOR 0x80 (an untouched byte, 0x80, reads as 0).
 // er_kv_read_blocks returns the GGUF blocks in their own order.
 // Quantiser (every step in float32, the same on every path that writes the
 // cache): amax = largest |x| of the block; d = fp16(amax / 127) (float32
@@ -59,7 +60,9 @@ __device__ inline void kvq_row(const float (&x)[E], int8_t *q_head, bool v, int 
     for (int e = 0; e < E; ++e) {
         float q = d > 0.f ? roundf(x[e] / d) : 0.f;
         q = fminf(fmaxf(q, -127.f), 127.f);
-        q_head[kvq_code_off(v, r, E * lane + e, 32 * E)] = (int8_t)(int)q;
+        // stored as q XOR 0x80 (as the repacked weights): one byte permute and one subtraction per pair
+        // turn a word of codes into exact fp16
+        q_head[kvq_code_off(v, r, E * lane + e, 32 * E)] = (int8_t)((uint8_t)(int8_t)(int)q ^ 0x80u);
     }
     if ((lane & (32 / E - 1)) == 0) d_row[lane / (32 / E)] = dh;
 }
