@@ -266,20 +266,23 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
                     kw[h][4 * k2] = w.x; kw[h][4 * k2 + 1] = w.y; kw[h][4 * k2 + 2] = w.z; kw[h][4 * k2 + 3] = w.w;
                 }
             }
-            // the K / V scales of this lane's four rows 2t, 2t + 1, 2t + 8, 2t + 9 (fp16 pairs)
-            const int rows4[4] = {2 * t, 2 * t + 1, 2 * t + 8, 2 * t + 9};
+            // the K / V scales of this lane's four rows 2t, 2t + 1, 2t + 8, 2t + 9 (fp16 pairs): rows 2t and
+            // 2t + 1 (and 2t + 8, 2t + 9) are adjacent, one 16- or 8-byte read per pair of rows and side
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int w = 0; w < HD / 64; ++w) {
-                    uint32_t x;
-                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x) : "r"(qslot + Q::QT + rows4[i] * Q::SROW + 4 * w));
-                    dks[i][w] = x;
-                    asm volatile("ld.shared.u32 %0, [%1];"
-                                 : "=r"(x)
-                                 : "r"(qslot + 2 * Q::QT + Q::ST + rows4[i] * Q::SROW + 4 * w));
-                    dvs[i][w] = x;
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t ko = qslot + Q::QT + (2 * t + 8 * pr) * Q::SROW;
+                const uint32_t vo = qslot + 2 * Q::QT + Q::ST + (2 * t + 8 * pr) * Q::SROW;
+                if constexpr (HD == 128) {
+                    const uint4 kx = lds128(ko), vx = lds128(vo);
+                    dks[2 * pr][0] = kx.x; dks[2 * pr][1] = kx.y; dks[2 * pr + 1][0] = kx.z; dks[2 * pr + 1][1] = kx.w;
+                    dvs[2 * pr][0] = vx.x; dvs[2 * pr][1] = vx.y; dvs[2 * pr + 1][0] = vx.z; dvs[2 * pr + 1][1] = vx.w;
+                } else {
+                    static_assert(HD == 64, "head dim 64 or 128");
+                    const uint2 kx = lds64(ko), vx = lds64(vo);
+                    dks[2 * pr][0] = kx.x; dks[2 * pr + 1][0] = kx.y;
+                    dvs[2 * pr][0] = vx.x; dvs[2 * pr + 1][0] = vx.y;
                 }
+            }
             slot = qslot;
             // scores block by block (2 k16 chunks per 32-value block), each block's sums times its row's scale
 #pragma unroll
