@@ -27,6 +27,15 @@
 // eight rows an ldmatrix reads together sit in eight different bank groups.
 // Two tiles per warp are in flight while a third is consumed; a range's first
 // two are requested before its queries are read.
+//
+// Q8_0 cache (template flag Q8; layout in kvq.cuh): whole 16-row tiles of the
+// code and scale planes are staged (rows outside the warp's range masked), and
+// each lane reads its B fragments as 32-bit words of codes, already in fragment
+// order, turning them into exact fp16 pairs in registers.  Score sums are kept
+// per 32-value block and multiplied by the row's K scale; for P V each block's
+// probabilities are multiplied by the row's V scale (and 2^8) before the hi/lo
+// split.  The warp whose range ends at a pair's last row first quantises the
+// step's new row from the fp32 staging into the planes.
 #include "common.cuh"
 #include "internal.h"
 #include "kvq.cuh"
