@@ -95,3 +95,6 @@ def test_null_arguments_rejected(er):
         er.er_kv_read_blocks(0, 0, 0, 0, 1, 0, 0, 0)
     assert e.value.status == er.ER_EINVAL
     assert er.er_kv_type(None) == -1
+    with pytest.raises(er.ErError) as e:
+        er.er_prefill(0, 0, 0, 1, 0, None, 0)
+    assert e.value.status == er.ER_EINVAL
