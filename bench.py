@@ -106,8 +106,8 @@ KERNEL_TRAFFIC = {
     ("llama2_7b_q4", "step_kernel"): ("3ef517f4638baae0", 5866404352 + 9216768),
     # attn_tc_kernel<128, 4, fp16 / Q8_0 cache>, 4th launch of `bench.py [--workload llama3_8b_q8_b16_kvq8]
     # --layers 1 --steps 1 --warmup 3 --no-cpu-baseline` (one layer: the per-layer shape of the full model)
-    ("llama3_8b_q8_b16", "attn"): ("593eddcf7d2052c6", 537753600 + 9616128),
-    ("llama3_8b_q8_b16_kvq8", "attn"): ("593eddcf7d2052c6", 291742208 + 9235200),
+    ("llama3_8b_q8_b16", "attn"): ("90937cb4d8f6371e", 537818880 + 9653504),
+    ("llama3_8b_q8_b16_kvq8", "attn"): ("90937cb4d8f6371e", 291743232 + 9249024),
 }
 
 

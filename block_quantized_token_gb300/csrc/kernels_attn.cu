@@ -26,7 +26,9 @@
 // 16-byte chunk c of row r is stored at chunk c ^ (r & 7) of the row, so the
 // eight rows an ldmatrix reads together sit in eight different bank groups.
 // Two tiles per warp are in flight while a third is consumed; a range's first
-// two are requested before its queries are read.
+// two are requested before its queries are read and, in decode with the fp16
+// cache, before the warp waits for the kernel that produced the queries and
+// the new row (unless those tiles hold the new row).
 //
 // Q8_0 cache (template flag Q8; layout in kvq.cuh): whole 16-row tiles of the
 // code and scale planes are staged (rows outside the warp's range masked), and
@@ -142,7 +144,7 @@ struct TaSrc {
 // cache holds Q8_0 blocks.
 template <int HD, int G, bool Q8>
 __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uint8_t *ring, int lane,
-                          TaState<HD> &st) {
+                          TaState<HD> &st, bool dep = false, bool last = false) {
     using C = TaCfg<HD>;
     using Q = TaQ8Cfg<HD>;
     const int g = lane >> 2, t = lane & 3;
@@ -189,7 +191,12 @@ __device__ void ta_attend(const float *qh, const TaSrc &src, int r0, int r1, uin
         }
         cp_async_commit();  // an empty group keeps the count uniform
     };
+    // dep: the producing kernel (queries, the new row) is still to be waited for.  The first tiles are requested
+    // before the wait unless they hold the new row, the pair's last (last: this piece ends the pair).
+    const bool pre = !(last && r1 - 1 < tb0 + (NS - 1) * TA_TILE);
+    if (dep && !pre) pdl_wait();
     for (int k = 0; k < NS - 1; ++k) issue(k);
+    if (dep && pre) pdl_wait();
     // queries: scale to log2 units, rescale by a power of two so that the lo
     // halves stay normal, split hi + lo into A fragments
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);
@@ -413,7 +420,10 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
     uint8_t *ring = smem + warp * (Q8 ? TaQ8Cfg<HD>::WARP : TA_SLOTS * C::SLOT);
     const int qd = a.H * HD;
 
-    pdl_wait();
+    // fp16 cache in decode: each warp waits for the producing kernel inside its first piece, after requesting
+    // tiles that kernel does not write
+    const bool defer = !Q8 && a.seqmap == nullptr;
+    if (!defer) pdl_wait();
     pdl_launch_dependents();
 
     // geometry of the row list (positions are inputs of the step)
@@ -434,6 +444,7 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
     const int wa = (int)((long long)w * geo.NR / geo.W), wb = (int)((long long)(w + 1) * geo.NR / geo.W);
 
     int u = wa;
+    bool dep = defer;
     while (u < wb) {
         int b, kvh, seg_start, seg_end;
         ta_locate(geo, a.B, u, b, kvh, seg_start, seg_end);
@@ -477,7 +488,9 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
             }
         }
         TaState<HD> st;
-        ta_attend<HD, G, Q8>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, src, r0, r1, ring, lane, st);
+        ta_attend<HD, G, Q8>(a.q + (size_t)b * qd + (size_t)kvh * G * HD, src, r0, r1, ring, lane, st, dep,
+                             r1 == seg_end - seg_start);
+        dep = false;
         float *o_grp = a.o + (size_t)b * qd + (size_t)kvh * G * HD;
         if (seg_start >= wa && seg_end <= wb) {  // the whole pair: finish here
             if (g < G) {
@@ -518,11 +531,11 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
             const int gi = (4 * ch) / HD, d = 4 * ch - gi * HD;
             float M = -INFINITY, L = 0.f;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w0 = w_first; w0 <= w_last; w0 += 8) {  // eight states in flight, online rescale
-                float mm[8], ll[8];
-                float4 ov[8];
+            for (int w0 = w_first; w0 <= w_last; w0 += 12) {  // twelve states in flight, online rescale
+                float mm[12], ll[12];
+                float4 ov[12];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 12; ++j) {
                     const int ww = w0 + j;
                     mm[j] = -INFINITY;
                     ll[j] = 0.f;
@@ -537,14 +550,14 @@ __global__ void __launch_bounds__(ta_warps(Q8) * 32, 1) attn_tc_kernel(const Att
                 }
                 float mc = M;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) mc = fmaxf(mc, mm[j]);
+                for (int j = 0; j < 12; ++j) mc = fmaxf(mc, mm[j]);
                 if (mc == -INFINITY) continue;
                 const float corr = exp2f(M - mc);
                 L *= corr;
                 O.x *= corr; O.y *= corr; O.z *= corr; O.w *= corr;
                 M = mc;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 12; ++j) {
                     const float ew = exp2f(mm[j] - mc);
                     L = fmaf(ll[j], ew, L);
                     O.x = fmaf(ov[j].x, ew, O.x); O.y = fmaf(ov[j].y, ew, O.y);
