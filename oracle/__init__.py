@@ -19,8 +19,11 @@ pages' default cache precision does; every other value is float64.
 Pins (tests/test_oracle_pins.py) tie each function to something other than
 itself: hand-built blocks with hand-derived values (tests/golden/), closed
 forms, invariants, torch float64 library routines, and cached-vs-uncached
-decoding.  The whole-step composition beyond those pins is "parity unpinned":
-the pages print no logits for any model.
+decoding.  The whole step is checked against a composition of torch float64
+routines (rms_norm, scaled_dot_product_attention with GQA, silu, RoPE as a
+complex rotation, struct-decoded blocks) on four small shapes.  No pin
+compares with output values the pages print: they print no logits for any
+model.
 """
 
 from .blocks import (BLOCK_BYTES, dequant, dequant_kv_q8_0, dequant_q4_0, dequant_q8_0, dequant_rows,  # noqa: F401
